@@ -1,0 +1,95 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each case edits one expression (always memory-safe for the shapes the pins use) of a copy of the oracle source (a dropped
+term, a wrong sign, a swapped index, ties rounded away from even ...),
+builds it into a throw-away library, swaps it in, and runs the pin tests.
+At least one pin must fail for every planted mistake.  The real oracle is
+restored afterwards.
+"""
+import inspect
+
+import pytest
+
+import oracle
+import test_oracle_cast as tc
+import test_oracle_codec as tk
+import test_oracle_scale as ts
+import test_oracle_swiglu as tw
+
+MUTATIONS = {
+    "ties_away_e4m3": ("(dropped == 0x80000u && (keep & 1u))",
+                       "(dropped == 0x80000u)"),
+    "ties_away_e2m1": ("(dropped == 0x200000u && (keep & 1u))",
+                       "(dropped == 0x200000u)"),
+    "subnormal_ties_away": ("(frac == 0.5f && (m & 1u))", "(frac == 0.5f)"),
+    "no_amax_floor": ("float a = amax > 1e-4f ? amax : 1e-4f;",
+                      "float a = amax;"),
+    "floor_1e3": ("amax > 1e-4f ? amax : 1e-4f", "amax > 1e-3f ? amax : 1e-3f"),
+    "sign_of_zero_lost": ("signbit(q) ? 0x80u : 0u", "q < 0 ? 0x80u : 0u"),
+    "pow2_exact_power_bumped": ("(f == 0.5f) ? E - 1 : E", "E"),
+    "subnormal_threshold": ("biased >= 127 - 6", "biased >= 127 - 7"),
+    "e4m3_bias": ("int e = biased - 127 + 7;", "int e = biased - 127 + 8;"),
+    "nibble_order": ("if ((col & 1) == 0)", "if ((col & 1) == 1)"),
+    "transposed_rows_paired": ("base[j * ld_scales + m] = sc.s;",
+                               "base[j * ld_scales + (m ^ 1)] = sc.s;"),
+    "ue8m0_byte_order": ("base[word * 4 + b] = (uint8_t)sc.ue8m0;",
+                         "base[word * 4 + (3 - b)] = (uint8_t)sc.ue8m0;"),
+    "ue8m0_pad_not_zeroed": ("base[word * 4 + b] = 0;", "(void)word;"),
+    "gate_up_swapped": ("row[k] = oracle_swiglu_value(bf16_bits_to_float(xr[k]),\n"
+                        "                                         bf16_bits_to_float(xr[N + k]));",
+                        "row[k] = oracle_swiglu_value(bf16_bits_to_float(xr[N + k]),\n"
+                        "                                         bf16_bits_to_float(xr[k]));"),
+    "silu_sign": ("(1.0 + exp(-g))", "(1.0 + exp(g))"),
+    "fmt_max_e2m1": ("448.0f : 6.0f", "448.0f : 8.0f"),
+    "scale_multiplied": ("float q = yg[k] / sc.s;", "float q = yg[k] * sc.s;"),
+    "amax_without_abs": ("float a = fabsf(yg[k]);", "float a = yg[k];"),
+    "saturation_dropped": ("if (a > 448.0f)\n        a = 448.0f;", ""),
+}
+
+
+def _pin_functions():
+    fns = []
+    for mod in (tk, ts, tc, tw):
+        for name, fn in inspect.getmembers(mod, inspect.isfunction):
+            if name.startswith("test_") and fn.__module__ == mod.__name__:
+                fns.append(fn)
+    return fns
+
+
+def _call_all_params(fn):
+    """Run a pin with every parametrisation pytest would give it."""
+    marks = getattr(fn, "pytestmark", [])
+    combos = [{}]
+    for m in marks:
+        if m.name != "parametrize":
+            continue
+        names = [n.strip() for n in m.args[0].split(",")]
+        new = []
+        for c in combos:
+            for v in m.args[1]:
+                vals = v if len(names) > 1 else (v,)
+                new.append({**c, **dict(zip(names, vals))})
+        combos = new
+    for kw in combos:
+        fn(**kw)
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = oracle.source_text()
+    assert old in src, f"mutation anchor not found: {old!r}"
+    lib = oracle.compile_variant(src.replace(old, new, 1),
+                                 str(tmp_path / f"lib_{name}.so"))
+    real = oracle._load()
+    oracle._lib = lib
+    failed = []
+    try:
+        for fn in _pin_functions():
+            try:
+                _call_all_params(fn)
+            except Exception:  # any failing pin counts
+                failed.append(fn.__name__)
+    finally:
+        oracle._lib = real
+    assert failed, f"no pin caught the planted mistake {name}"
