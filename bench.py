@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 per-token group-wise cast.
+
+One step = one pass of the whole cast (load, group amax, scale, quantize,
+store codes, store scales -- all in one kernel launch) over one batch: the
+4096 x 7168 BF16 -> FP8 E4M3, group 128, UE8M0-packed workload by default.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2]
+    python bench.py --impl reference ...     # the CPU oracle as the baseline
+
+Timing: W untimed warm-up steps, then exactly K timed steps between a
+barrier + cuda synchronize on both sides.  Before every step the L2 is
+flushed by writing a buffer of twice its size (outside the timed interval);
+each step's kernel is bracketed by CUDA events on its launching stream, and
+ms_per_step is their mean (max over ranks).  N > 1 runs one independent
+replica of the workload per GPU (rows are independent: no collective on the
+data path), so scaling is weak and value = bytes of all ranks / that time.
+
+Prints ONE JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from precision_quantization_token_gb300.inputs import (WORKLOADS,  # noqa: E402
+                                                       make_input)
+
+METRIC = "per-token cast GB/s (in+out bytes) and % of GB300 HBM peak at 4096x7168"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "per_token_cast_c2_traffic.txt")
+
+
+# ------------------------------------------------------------------ utils
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--per-config-steps", type=int, default=2000,
+                    help="timed steps for each of the other workloads "
+                         "(0 disables the per-config table)")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--flush", default="write", choices=["write", "write+read"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU time budget of the oracle baseline sample")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(
+        ROOT, "precision_quantization_token_gb300", "csrc", "*"))) + \
+        sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for p in files:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source and the same workload (else None)."""
+    try:
+        fields = {}
+        with open(PROFILE_TRAFFIC) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256") != kernel_source_hash():
+            return None
+        if fields.get("workload") != workload:
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}",
+                 f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None,
+                    "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- GPU arm
+
+class GpuWorkload:
+    """Device buffers for one workload and a launcher through the C ABI."""
+
+    def __init__(self, w, torch, tk, device):
+        self.w, self.torch, self.tk = w, torch, tk
+        self.bits = make_input(w)
+        self.x = torch.from_numpy(self.bits.view(np.int16)).view(
+            torch.bfloat16).to(device)
+        row_bytes = w.K if w.fmt == "e4m3" else w.K // 2
+        self.codes = torch.empty((w.M, row_bytes), dtype=torch.uint8,
+                                 device=device)
+        shape, dt = tk.scale_shape(w.M, w.K, w.group, w.scale, w.layout)
+        self.scales = torch.empty(shape, dtype=getattr(torch, dt),
+                                  device=device)
+        self.entry = (tk.tk_swiglu_per_token_cast if w.swiglu
+                      else tk.tk_per_token_cast)
+        self.bytes = w.algorithmic_bytes()
+
+    def launch(self, stream_handle):
+        w, tk = self.w, self.tk
+        self.entry(self.x.data_ptr(), w.M, w.K, self.x.stride(0), w.group,
+                   tk.FMT[w.fmt], tk.SCALE[w.scale], tk.LAYOUT[w.layout],
+                   self.codes.data_ptr(), self.codes.stride(0),
+                   self.scales.data_ptr(), self.scales.stride(0),
+                   stream_handle)
+
+
+def time_steps(torch, wl, steps, warmup, flush_buf, flush_read, world):
+    """Per-step kernel times (ms) with the L2 flushed before each step."""
+    stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream
+
+    def flush():
+        flush_buf.zero_()
+        if flush_read is not None:
+            flush_read.sum(dtype=torch.float32)
+
+    for _ in range(warmup):
+        flush()
+        wl.launch(handle)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        wl.launch(handle)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return ms, wall
+
+
+def run_gpu(args):
+    import torch
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    import precision_quantization_token_gb300 as tk
+    tk.load()
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    flush_read = (torch.ones(2 * l2 // 2, dtype=torch.bfloat16, device=device)
+                  if args.flush == "write+read" else None)
+
+    w = WORKLOADS[args.workload]
+    wl = GpuWorkload(w, torch, tk, device)
+    peak, peak_src = measured_peaks()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ms, wall = time_steps(torch, wl, args.steps, args.warmup, flush_buf,
+                          flush_read, world)
+    clock_info = clocks.stop()
+
+    mean_ms = statistics.fmean(ms)
+    mean_ms_all = reduce_max(mean_ms, world)
+    total_bytes = wl.bytes["total"] * world
+    value = total_bytes / (mean_ms_all * 1e-3) / 1e9
+    achieved = wl.bytes["total"] / (mean_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean_ms_all, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64, BF16-rounded)",
+        "config": {
+            "workload": w.describe(), "name": w.name, "M": w.M, "K": w.K,
+            "group": w.group, "fmt": w.fmt, "scale": w.scale,
+            "layout": w.layout, "swiglu": w.swiglu, "seed": w.seed,
+            "bytes_per_step": wl.bytes,
+            "l2": f"flushed before every step by writing {2 * l2 >> 20} MiB"
+                  + (" then reading 2x L2" if flush_read is not None else "")
+                  + " (outside the timed events)",
+            "timing": "CUDA events around each launch on its stream; mean "
+                      "of the steps; max over ranks",
+            "median_ms": round(statistics.median(ms), 6),
+            "min_ms": round(min(ms), 6),
+            "wall_s_timed_region": round(wall, 3),
+            "parallelism": f"replicas x{world} (rows independent)"},
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 2),
+            "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(w.name), "peak_source": peak_src,
+            "kernel": "per_token_cast_kernel"},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+
+    if rank == 0 and args.per_config_steps > 0:
+        table = {}
+        for name in sorted(WORKLOADS):
+            if name == w.name:
+                continue
+            other = GpuWorkload(WORKLOADS[name], torch, tk, device)
+            oms, _ = time_steps(torch, other, args.per_config_steps,
+                                max(3, args.warmup // 5), flush_buf,
+                                flush_read, 1)
+            m = statistics.fmean(oms)
+            gbps = other.bytes["total"] / (m * 1e-3) / 1e9
+            table[name] = {"workload": other.w.describe(),
+                           "ms": round(m, 6), "GB/s": round(gbps, 1),
+                           "frac_of_peak": round(gbps / peak, 4),
+                           "bytes": other.bytes["total"]}
+            del other
+        result["per_config"] = table
+
+    if args.e2e_steps > 0:
+        result["e2e"] = run_e2e(torch, tk, w, args.e2e_steps, device, world)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(torch, tk, w, steps, device, world):
+    """Same metric through the public API with host buffers: each step copies
+    the pinned host input to the device, casts, and copies codes and scales
+    back to pinned host memory (all inside the timed interval)."""
+    bits = make_input(w)
+    xh = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    xh = xh.pin_memory()
+    row_bytes = w.K if w.fmt == "e4m3" else w.K // 2
+    codes = torch.empty((w.M, row_bytes), dtype=torch.uint8, pin_memory=True)
+    shape, dt = tk.scale_shape(w.M, w.K, w.group, w.scale, w.layout)
+    scales = torch.empty(shape, dtype=getattr(torch, dt), pin_memory=True)
+    fn = tk.swiglu_per_token_cast if w.swiglu else tk.per_token_cast
+    for _ in range(3):
+        fn(xh, w.group, w.fmt, w.scale, w.layout, codes=codes, scales=scales)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        fn(xh, w.group, w.fmt, w.scale, w.layout, codes=codes, scales=scales)
+    torch.cuda.synchronize()
+    barrier(world)
+    dt_s = reduce_max((time.perf_counter() - t0) / steps, world)
+    b = w.algorithmic_bytes()
+    return {"value": round(b["total"] * world / dt_s / 1e9, 2), "unit": UNIT,
+            "ms_per_step": round(dt_s * 1e3, 4),
+            "h2d_bytes_per_step": int(xh.numel() * 2),
+            "d2h_bytes_per_step": int(codes.numel() + scales.numel() * 4),
+            "api": ("precision_quantization_token_gb300."
+                    + ("swiglu_per_token_cast" if w.swiglu
+                       else "per_token_cast") + " on pinned host tensors")}
+
+
+# ------------------------------------------------------------- CPU arm
+
+def cpu_baseline(w, seconds: float):
+    """The oracle as it stands, on all host cores, over whole passes of the
+    workload (or a leading block of rows when one pass would exceed the
+    budget); GB/s over the same algorithmic bytes."""
+    import oracle
+    threads = oracle.host_threads()
+    fmt = oracle.FMT_E4M3 if w.fmt == "e4m3" else oracle.FMT_E2M1
+    mode = {"fp32": oracle.SCALE_FP32, "pow2": oracle.SCALE_FP32_POW2,
+            "ue8m0": oracle.SCALE_UE8M0}[w.scale]
+    layout = (oracle.LAYOUT_ROW_MAJOR if w.layout == "row"
+              else oracle.LAYOUT_TRANSPOSED)
+    fn = oracle.swiglu_per_token_cast if w.swiglu else oracle.per_token_cast
+    # probe on a small block to size the sample
+    probe_rows = max(threads, min(w.M, 256))
+    bits = make_input(w, M=probe_rows) if probe_rows < w.M else make_input(w)
+    t0 = time.perf_counter()
+    fn(bits[:probe_rows], w.K, w.group, fmt, mode, layout, threads=threads)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    rows = int(min(w.M, max(probe_rows, seconds / max(per_row, 1e-9))))
+    sample = make_input(w, M=rows) if rows < w.M else make_input(w)
+    passes, elapsed = 0, 0.0
+    t0 = time.perf_counter()
+    while True:
+        fn(sample, w.K, w.group, fmt, mode, layout, threads=threads)
+        passes += 1
+        elapsed = time.perf_counter() - t0
+        if elapsed >= min(seconds, 3.0) or passes >= 1000:
+            break
+    frac = rows / w.M
+    gb = w.algorithmic_bytes()["total"] * frac * passes / 1e9
+    return {"value": round(gb / elapsed, 3), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": (f"{rows} of {w.M} rows of the workload, {passes} "
+                       f"pass(es), {elapsed:.2f} s wall on {threads} threads")}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    import oracle
+    threads = oracle.host_threads()
+    fmt = oracle.FMT_E4M3 if w.fmt == "e4m3" else oracle.FMT_E2M1
+    mode = {"fp32": oracle.SCALE_FP32, "pow2": oracle.SCALE_FP32_POW2,
+            "ue8m0": oracle.SCALE_UE8M0}[w.scale]
+    layout = (oracle.LAYOUT_ROW_MAJOR if w.layout == "row"
+              else oracle.LAYOUT_TRANSPOSED)
+    fn = oracle.swiglu_per_token_cast if w.swiglu else oracle.per_token_cast
+    # each step is a bounded sample of rows sized so that the whole run
+    # stays within a few minutes
+    budget_s = 120.0 / max(1, args.steps + args.warmup)
+    probe_rows = min(w.M, max(threads, 64))
+    probe = make_input(w, M=probe_rows)
+    t0 = time.perf_counter()
+    fn(probe, w.K, w.group, fmt, mode, layout, threads=threads)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    rows = int(min(w.M, max(1, budget_s / max(per_row, 1e-9))))
+    sample = make_input(w, M=rows) if rows < w.M else make_input(w)
+    for _ in range(args.warmup):
+        fn(sample, w.K, w.group, fmt, mode, layout, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn(sample, w.K, w.group, fmt, mode, layout, threads=threads)
+    dt_s = (time.perf_counter() - t0) / args.steps
+    gb = w.algorithmic_bytes()["total"] * rows / w.M / 1e9
+    value = round(gb / dt_s, 3)
+    sample_desc = (f"{rows} of {w.M} rows per step, {threads} threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt_s * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64, BF16-rounded)",
+        "config": {"workload": w.describe(), "name": w.name, "M": w.M,
+                   "K": w.K, "group": w.group},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample_desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

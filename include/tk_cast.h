@@ -1,0 +1,139 @@
+/*
+ * tk_cast.h -- C ABI of the GB300 per-token group-wise activation cast.
+ *
+ * The operation (TileKernels README, section "Features": "per-token ...
+ * FP8/FP4 casting ... with fused SwiGLU+quantization"; aiwiki "TileKernels",
+ * section "Quantization": scale-factor groups of 16, 32, 64 or 128 channels,
+ * power-of-two rounding of scale factors, packed UE8M0 scale factors, and
+ * per-token scale factors "in DeepGEMM's layout"):
+ *
+ *   for every row m (a token) and every group j of `group` consecutive
+ *   channels of that row:
+ *     amax  = max |x[m, k]| over the group           (fp32, exact)
+ *     r     = max(amax, 1e-4f) / fmt_max              (one IEEE fp32 division)
+ *     scale = r                      (TK_SCALE_FP32)
+ *           = 2^ceil(log2 r)         (TK_SCALE_FP32_POW2, TK_SCALE_UE8M0_PACKED)
+ *     code  = round-to-nearest-even(saturate(x / scale, +-fmt_max))
+ *             with x / scale one IEEE fp32 division (for a power-of-two scale
+ *             the exact product by 2^-k, which is the same number)
+ *   fmt_max = 448 for FP8 E4M3 (OCP E4M3FN), 6 for FP4 E2M1 (OCP MX).
+ *   The sign of x is kept on every code, zeros included.
+ *
+ * Conventions shared by every entry point:
+ *  - All data pointers are DEVICE pointers (global memory of the current
+ *    CUDA device).  The caller allocates and owns every buffer; the library
+ *    allocates nothing and keeps no pointer after the call returns.
+ *  - Calls are asynchronous: they validate on the host, enqueue one kernel
+ *    on `stream` (a cudaStream_t passed as void*, NULL = legacy default
+ *    stream) and return.  Outputs are ready once the stream reaches that
+ *    point.  Input and outputs must not overlap.
+ *  - Inputs must be finite; NaN/Inf inputs give unspecified codes/scales.
+ *  - Errors are returned, never raised: nothing aborts or throws across
+ *    the ABI, and nothing is launched when a check fails.
+ *  - Alignment (TK_ERR_MISALIGNED otherwise; there is no scalar fallback):
+ *    x and codes 16-byte aligned; row strides ld_x * 2 bytes and ld_codes
+ *    bytes multiples of 16; scales 4-byte aligned; for the transposed layout
+ *    ld_scales a multiple of 4 (16-byte aligned scale rows).
+ *  - Entries of the scale tensor outside the written region (row-major
+ *    columns past the last word, transposed columns m >= M) are left
+ *    untouched, as are code bytes past each row's K (or K/2) bytes.
+ *  - M == 0 is a no-op that returns TK_OK without looking at the pointers.
+ *  - Limits: 0 <= M <= 2^30, K (or N) <= 2^28 (TK_ERR_UNSUPPORTED beyond).
+ */
+#ifndef TK_CAST_H
+#define TK_CAST_H
+
+#include <stdint.h>
+
+/* Exported from the shared library even when it is built with hidden
+ * default visibility. */
+#if defined(__GNUC__)
+#define TK_API __attribute__((visibility("default")))
+#else
+#define TK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TK_OK = 0,
+    TK_ERR_INVALID_ARG = 1,  /* bad enum, group, shape, stride or null ptr */
+    TK_ERR_UNSUPPORTED = 2,  /* a size beyond the stated limits */
+    TK_ERR_MISALIGNED = 3,   /* pointer or stride breaks the alignment rule */
+    TK_ERR_CUDA = 4          /* the launch failed (see tk_last_cuda_error) */
+} tk_status;
+
+typedef enum {
+    TK_FMT_E4M3 = 0,  /* FP8 E4M3FN, 1 byte per code */
+    TK_FMT_E2M1 = 1   /* FP4 E2M1, 2 codes per byte, element 2i in bits 3:0 */
+} tk_format;
+
+typedef enum {
+    TK_SCALE_FP32 = 0,         /* fp32 scale r */
+    TK_SCALE_FP32_POW2 = 1,    /* fp32 scale 2^k, the smallest power of two >= r */
+    TK_SCALE_UE8M0_PACKED = 2  /* the byte 127 + k, four per int32 word:
+                                  group 4w+b in byte b of word w (little endian);
+                                  unused bytes of a partial last word are 0 */
+} tk_scale_mode;
+
+typedef enum {
+    /* [M][ld_scales] words: ld_scales >= G (fp32) or ceil(G/4) (packed). */
+    TK_SCALE_ROW_MAJOR = 0,
+    /* DeepGEMM's per-token layout: [G or ceil(G/4)][ld_scales] words with
+     * ld_scales >= M and a multiple of 4 (M padded, e.g. M_pad = ceil(M/4)*4).
+     * Word (j, m) holds row m's scale of group j (packed: groups 4j..4j+3). */
+    TK_SCALE_TRANSPOSED_PADDED = 1
+} tk_scale_layout;
+
+/*
+ * tk_per_token_cast -- per-token group-wise cast of a BF16 matrix.
+ *
+ *   x         BF16 [M][ld_x] row-major, K values used per row.
+ *   M, K      rows (tokens) and channels; K % group == 0.
+ *   ld_x      input row stride in elements, >= K.
+ *   group     channels per scale: 16, 32, 64 or 128.
+ *   fmt       tk_format.  mode: tk_scale_mode.  layout: tk_scale_layout.
+ *   codes     uint8 [M][ld_codes]: K bytes (E4M3) or K/2 bytes (E2M1) per row.
+ *   ld_codes  code row stride in bytes, >= the row's code bytes.
+ *   scales    fp32 or int32 words laid out per `layout`, G = K / group.
+ *   ld_scales scale row stride in 4-byte words (see tk_scale_layout).
+ *   stream    cudaStream_t as void*.
+ */
+TK_API tk_status tk_per_token_cast(const void *x, int64_t M, int64_t K, int64_t ld_x,
+                            int group, int fmt, int mode, int layout,
+                            void *codes, int64_t ld_codes, void *scales,
+                            int64_t ld_scales, void *stream);
+
+/*
+ * tk_swiglu_per_token_cast -- fused SwiGLU + per-token cast (TileKernels
+ * README, "Features": "fused SwiGLU+quantization ops"; the activation and the
+ * narrowing happen in one pass with no intermediate tensor in memory).
+ *
+ *   x         BF16 [M][ld_x], row m = [gate (N values) | up (N values)].
+ *   y[m, k] = silu(gate[m, k]) * up[m, k] = gate*up / (1 + e^-gate), in fp32,
+ *   then cast exactly as tk_per_token_cast casts a row of K = N values.
+ *   ld_x >= 2N.  Other arguments as for tk_per_token_cast with K = N.
+ *   The fp32 product is within a few ulps of the correctly rounded one (it
+ *   uses expf and one IEEE division), so a code can differ by one step from
+ *   a cast of the exactly rounded product.
+ */
+TK_API tk_status tk_swiglu_per_token_cast(const void *x, int64_t M, int64_t N,
+                                   int64_t ld_x, int group, int fmt, int mode,
+                                   int layout, void *codes, int64_t ld_codes,
+                                   void *scales, int64_t ld_scales,
+                                   void *stream);
+
+/* Static string naming a status value ("TK_OK", ...). */
+TK_API const char *tk_status_string(int status);
+
+/* Text of the CUDA error behind the calling thread's most recent
+ * TK_ERR_CUDA, or "" if there was none.  Static or thread-local storage. */
+TK_API const char *tk_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TK_CAST_H */

@@ -38,6 +38,8 @@ LAYOUT_ROW_MAJOR, LAYOUT_TRANSPOSED = 0, 1
 
 _lib = None
 _lock = threading.Lock()
+_pool = None
+_pool_size = 0
 
 
 def build(force: bool = False) -> str:
@@ -68,6 +70,8 @@ def _configure(lib):
     lib.oracle_encode.restype = None
     lib.oracle_scale.argtypes = [p, i64, i, i, p, p]
     lib.oracle_scale.restype = None
+    lib.oracle_swiglu_values.argtypes = [p, i64, i64, i64, i64, p, i64]
+    lib.oracle_swiglu_values.restype = None
     return lib
 
 
@@ -94,6 +98,18 @@ def compile_variant(src_text: str, out_path: str):
 def source_text() -> str:
     with open(_SRC) as f:
         return f.read()
+
+
+def _executor(threads: int) -> ThreadPoolExecutor:
+    """A process-wide thread pool, reused across calls (grown on demand)."""
+    global _pool, _pool_size
+    with _lock:
+        if _pool is None or _pool_size < threads:
+            if _pool is not None:
+                _pool.shutdown(wait=False)
+            _pool = ThreadPoolExecutor(threads)
+            _pool_size = threads
+        return _pool
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -132,8 +148,7 @@ def _run(fn, x, n_rows, K_or_N, ld_x, group, fmt, mode, layout, codes,
     if threads == 1:
         rcs = [work(0)]
     else:
-        with ThreadPoolExecutor(threads) as ex:
-            rcs = list(ex.map(work, range(threads)))
+        rcs = list(_executor(threads).map(work, range(threads)))
     for rc in rcs:
         if rc != 0:
             raise ValueError(f"oracle returned status {rc}")
@@ -178,6 +193,26 @@ def swiglu_per_token_cast(x_bits: np.ndarray, N: int, group: int, fmt: int,
     _run(lib.oracle_swiglu_per_token_cast, x_bits, M, N, ld_x, group, fmt,
          mode, layout, codes, scales, threads)
     return codes, scales
+
+
+def swiglu_values(x_bits: np.ndarray, N: int, threads: int = 1) -> np.ndarray:
+    """The fp32 SwiGLU product [M, N] of x_bits = [gate | up] (no cast)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, ld_x = x_bits.shape
+    y = np.empty((M, N), np.float32)
+    lib = _load()
+    threads = max(1, min(threads or 1, M))
+    bounds = np.linspace(0, M, threads + 1).astype(np.int64)
+
+    def work(t):
+        lib.oracle_swiglu_values(_ptr(x_bits), int(bounds[t]),
+                                 int(bounds[t + 1]), N, ld_x, _ptr(y), N)
+
+    if threads == 1:
+        work(0)
+    else:
+        list(_executor(threads).map(work, range(threads)))
+    return y
 
 
 def swiglu_value(gate: float, up: float) -> float:

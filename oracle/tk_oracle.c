@@ -347,6 +347,18 @@ int oracle_swiglu_per_token_cast(const uint16_t *x, int64_t m_begin,
     return rc;
 }
 
+/* The fp32 SwiGLU product rows alone (no cast): y row m at y + m*ld_y. */
+void oracle_swiglu_values(const uint16_t *x, int64_t m_begin, int64_t m_end,
+                          int64_t N, int64_t ld_x, float *y, int64_t ld_y)
+{
+    for (int64_t m = m_begin; m < m_end; ++m) {
+        const uint16_t *xr = x + m * ld_x;
+        for (int64_t k = 0; k < N; ++k)
+            y[m * ld_y + k] = oracle_swiglu_value(bf16_bits_to_float(xr[k]),
+                                                  bf16_bits_to_float(xr[N + k]));
+    }
+}
+
 /* ------------------------------------------- element-level hooks for pins */
 
 /* Saturating RNE encode of n fp32 values (the code step of the cast alone). */

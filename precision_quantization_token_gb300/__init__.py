@@ -1,0 +1,197 @@
+"""GB300-native per-token group-wise activation cast (BF16 -> FP8 E4M3 / FP4 E2M1).
+
+Thin Python binding over the C-ABI library built from ``csrc/`` (declared in
+``include/tk_cast.h``).  The binding only marshals arguments: PyTorch provides
+device memory and the current stream, and every step of the cast runs in the
+library's CUDA kernel.  There is no CPU fallback: if the library is missing,
+every call raises.
+
+Low level (same names and arguments as the C ABI, raw pointers and sizes):
+    tk_per_token_cast(x_ptr, M, K, ld_x, group, fmt, mode, layout,
+                      codes_ptr, ld_codes, scales_ptr, ld_scales, stream)
+    tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, ...)
+
+Tensor level (allocates outputs with torch):
+    codes, scales = per_token_cast(x, group=128, fmt="e4m3", scale="fp32",
+                                   layout="row")
+    codes, scales = swiglu_per_token_cast(x, group=128, ...)  # x = [gate|up]
+
+Operation (TileKernels README, "Features"; aiwiki "TileKernels", section
+"Quantization"): per row and per group of 16/32/64/128 channels, amax, a
+scale max(amax, 1e-4)/fmt_max (fp32, or rounded up to 2^k, optionally packed
+as UE8M0 bytes four per int32), and round-to-nearest-even saturated codes;
+scales row-major or transposed with M padded ("DeepGEMM's layout").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+FMT = {"e4m3": 0, "e2m1": 1}
+SCALE = {"fp32": 0, "pow2": 1, "ue8m0": 2}
+LAYOUT = {"row": 0, "transposed": 1}
+
+TK_OK = 0
+STATUS_NAMES = {0: "TK_OK", 1: "TK_ERR_INVALID_ARG", 2: "TK_ERR_UNSUPPORTED",
+                3: "TK_ERR_MISALIGNED", 4: "TK_ERR_CUDA"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class TkError(RuntimeError):
+    """A non-OK status returned by the library."""
+
+    def __init__(self, status: int, detail: str = ""):
+        self.status = status
+        name = STATUS_NAMES.get(status, f"status {status}")
+        super().__init__(f"{name}{': ' + detail if detail else ''}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (in-tree)."""
+    return _build.build(force=force)
+
+
+def load():
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library not built ({path} missing); run "
+                    "precision_quantization_token_gb300.build() first")
+            lib = ctypes.CDLL(path)
+            i64, p, i = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+            sig = [p, i64, i64, i64, i, i, i, i, p, i64, p, i64, p]
+            for name in ("tk_per_token_cast", "tk_swiglu_per_token_cast"):
+                fn = getattr(lib, name)
+                fn.argtypes = sig
+                fn.restype = i
+            lib.tk_status_string.argtypes = [i]
+            lib.tk_status_string.restype = ctypes.c_char_p
+            lib.tk_last_cuda_error.argtypes = []
+            lib.tk_last_cuda_error.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != TK_OK:
+        detail = ""
+        if status == 4:
+            detail = load().tk_last_cuda_error().decode()
+        raise TkError(status, detail)
+
+
+# ------------------------------------------------------------- C-ABI names
+
+def tk_per_token_cast(x_ptr, M, K, ld_x, group, fmt, mode, layout, codes_ptr,
+                      ld_codes, scales_ptr, ld_scales, stream=0) -> None:
+    """Raw-pointer call of the C entry point; raises TkError on failure."""
+    _check(load().tk_per_token_cast(x_ptr, M, K, ld_x, group, fmt, mode,
+                                    layout, codes_ptr, ld_codes, scales_ptr,
+                                    ld_scales, stream))
+
+
+def tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, group, fmt, mode, layout,
+                             codes_ptr, ld_codes, scales_ptr, ld_scales,
+                             stream=0) -> None:
+    """Raw-pointer call of the fused SwiGLU entry point."""
+    _check(load().tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, group, fmt,
+                                           mode, layout, codes_ptr, ld_codes,
+                                           scales_ptr, ld_scales, stream))
+
+
+def tk_status_string(status: int) -> str:
+    return load().tk_status_string(status).decode()
+
+
+# ---------------------------------------------------------- tensor helpers
+
+def scale_shape(M: int, K: int, group: int, scale: str = "fp32",
+                layout: str = "row", m_pad_to: int = 4):
+    """Shape and torch dtype name of the scale tensor for an [M, K] cast."""
+    G = K // group
+    words = (G + 3) // 4 if scale == "ue8m0" else G
+    dtype = "int32" if scale == "ue8m0" else "float32"
+    if layout == "row":
+        return (M, words), dtype
+    m_pad = (M + m_pad_to - 1) // m_pad_to * m_pad_to
+    return (words, m_pad), dtype
+
+
+def _outputs(torch, M, K, group, fmt, scale, layout, device, codes, scales):
+    row_bytes = K if fmt == "e4m3" else K // 2
+    if codes is None:
+        codes = torch.empty((M, row_bytes), dtype=torch.uint8, device=device)
+    if scales is None:
+        shape, dt = scale_shape(M, K, group, scale, layout)
+        scales = torch.empty(shape, dtype=getattr(torch, dt), device=device)
+    return codes, scales
+
+
+def _call(entry, x, K, group, fmt, scale, layout, codes, scales, stream):
+    import torch
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 tensor with unit column "
+                         "stride")
+    on_host = x.device.type == "cpu"
+    xd = x.to("cuda", non_blocking=True) if on_host else x
+    M = xd.shape[0]
+    dev_codes, dev_scales = _outputs(torch, M, K, group, fmt, scale, layout,
+                                     xd.device, None if on_host else codes,
+                                     None if on_host else scales)
+    if stream is None:
+        stream = torch.cuda.current_stream(xd.device).cuda_stream
+    entry(xd.data_ptr(), M, K, xd.stride(0), group, FMT[fmt], SCALE[scale],
+          LAYOUT[layout], dev_codes.data_ptr(), dev_codes.stride(0),
+          dev_scales.data_ptr(), dev_scales.stride(0), stream)
+    if not on_host:
+        return dev_codes, dev_scales
+    if codes is None:
+        codes = torch.empty(dev_codes.shape, dtype=dev_codes.dtype,
+                            pin_memory=True)
+    if scales is None:
+        scales = torch.empty(dev_scales.shape, dtype=dev_scales.dtype,
+                             pin_memory=True)
+    codes.copy_(dev_codes, non_blocking=True)
+    scales.copy_(dev_scales, non_blocking=True)
+    torch.cuda.current_stream(xd.device).synchronize()
+    return codes, scales
+
+
+def per_token_cast(x, group: int = 128, fmt: str = "e4m3",
+                   scale: str = "fp32", layout: str = "row", *, codes=None,
+                   scales=None, stream=None):
+    """Per-token group-wise cast of a bfloat16 [M, K] tensor.
+
+    CUDA input: outputs are CUDA tensors, the call is asynchronous on the
+    current stream.  CPU input (preferably pinned): the input is copied to
+    the current CUDA device, cast there, and the outputs are copied back into
+    (pinned) host tensors before returning.
+    Returns (codes uint8 [M, K or K/2], scales) -- see ``scale_shape``.
+    """
+    K = x.shape[1]
+    return _call(tk_per_token_cast, x, K, group, fmt, scale, layout, codes,
+                 scales, stream)
+
+
+def swiglu_per_token_cast(x, group: int = 128, fmt: str = "e4m3",
+                          scale: str = "fp32", layout: str = "row", *,
+                          codes=None, scales=None, stream=None):
+    """Fused SwiGLU + per-token cast of x = [gate | up] (bfloat16 [M, 2N])."""
+    if x.shape[1] % 2:
+        raise ValueError("x must hold [gate | up] halves of equal width")
+    N = x.shape[1] // 2
+    return _call(tk_swiglu_per_token_cast, x, N, group, fmt, scale, layout,
+                 codes, scales, stream)

@@ -1,0 +1,119 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before any CUDA call (CPU only: no kernel runs)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import precision_quantization_token_gb300 as tk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+A = 0x10000          # fake, 16-byte aligned "device" addresses: never touched
+B = 0x20000
+C = 0x30000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tk.build()
+    return tk.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(tk_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "tk_per_token_cast" in names and "tk_swiglu_per_token_cast" in names
+    raw = ctypes.CDLL(tk.library_path())
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    assert tk.tk_status_string(0) == "TK_OK"
+    assert tk.tk_status_string(3) == "TK_ERR_MISALIGNED"
+    assert tk.tk_status_string(99) == "TK_ERR_UNKNOWN"
+    assert lib.tk_last_cuda_error() == b""
+
+
+def call(lib, *, x=A, M=4, K=256, ld_x=256, group=128, fmt=0, mode=0,
+         layout=0, codes=B, ld_codes=256, scales=C, ld_scales=2, swiglu=False):
+    fn = lib.tk_swiglu_per_token_cast if swiglu else lib.tk_per_token_cast
+    return fn(x, M, K, ld_x, group, fmt, mode, layout, codes, ld_codes, scales,
+              ld_scales, None)
+
+
+CASES = [
+    ("bad group", dict(group=48), INVALID),
+    ("group 8", dict(group=8), INVALID),
+    ("K not multiple of group", dict(K=200, ld_x=256), INVALID),
+    ("K zero", dict(K=0), INVALID),
+    ("negative M", dict(M=-1), INVALID),
+    ("bad fmt", dict(fmt=2), INVALID),
+    ("bad mode", dict(mode=3), INVALID),
+    ("bad layout", dict(layout=2), INVALID),
+    ("ld_x < K", dict(ld_x=128), INVALID),
+    ("ld_codes < K", dict(ld_codes=128), INVALID),
+    ("e2m1 ld_codes < K/2", dict(fmt=1, ld_codes=112), INVALID),
+    ("row scales too narrow", dict(ld_scales=1), INVALID),
+    ("packed scales too narrow", dict(mode=2, K=1280, ld_x=1280,
+                                      ld_codes=1280, ld_scales=2), INVALID),
+    ("transposed ld < M", dict(layout=1, M=8, ld_scales=4), INVALID),
+    ("null x", dict(x=None), INVALID),
+    ("null codes", dict(codes=None), INVALID),
+    ("null scales", dict(scales=None), INVALID),
+    ("x misaligned", dict(x=A + 8), MISALIGNED),
+    ("ld_x not 16 bytes", dict(K=128, ld_x=132), MISALIGNED),
+    ("codes misaligned", dict(codes=B + 4), MISALIGNED),
+    ("ld_codes not 16", dict(ld_codes=264), MISALIGNED),
+    ("scales misaligned", dict(scales=C + 2), MISALIGNED),
+    ("transposed ld not multiple of 4", dict(layout=1, M=5, ld_scales=5),
+     MISALIGNED),
+    ("M too large", dict(M=(1 << 30) + 1), UNSUPPORTED),
+    ("K too large", dict(K=(1 << 28) + 128, ld_x=(1 << 28) + 128,
+                         ld_codes=(1 << 28) + 128, ld_scales=1 << 22),
+     UNSUPPORTED),
+    ("swiglu ld_x < 2N", dict(swiglu=True, ld_x=384), INVALID),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", CASES, ids=[c[0] for c in CASES])
+def test_validation(lib, name, kw, want):
+    assert call(lib, **kw) == want
+
+
+def test_empty_batch_is_a_noop(lib):
+    assert call(lib, M=0, x=None, codes=None, scales=None) == OK
+    assert call(lib, M=0, x=None, codes=None, scales=None, swiglu=True,
+                ld_x=512) == OK
+
+
+def test_python_wrapper_raises(lib):
+    with pytest.raises(tk.TkError) as e:
+        tk.tk_per_token_cast(A, 4, 256, 256, 48, 0, 0, 0, B, 256, C, 2, 0)
+    assert e.value.status == INVALID
+
+
+def test_product_package_does_not_touch_the_oracle():
+    """The product package imports nothing from oracle/ (and vice versa)."""
+    pkg = os.path.join(ROOT, "precision_quantization_token_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*.*"), recursive=True):
+        if path.endswith((".py", ".cu", ".cuh", ".h")):
+            src = open(path).read()
+            assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), path
+            assert "tk_oracle" not in src, path
+    for path in glob.glob(os.path.join(ROOT, "oracle", "*.*")):
+        if path.endswith((".py", ".c")):
+            src = open(path).read()
+            assert "import precision_quantization_token_gb300" not in src
+            assert "from precision_quantization_token_gb300" not in src
+            assert "tk_cast.h" not in src
