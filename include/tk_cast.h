@@ -115,9 +115,12 @@ TK_API tk_status tk_per_token_cast(const void *x, int64_t M, int64_t K, int64_t 
  *   y[m, k] = silu(gate[m, k]) * up[m, k] = gate*up / (1 + e^-gate), in fp32,
  *   then cast exactly as tk_per_token_cast casts a row of K = N values.
  *   ld_x >= 2N.  Other arguments as for tk_per_token_cast with K = N.
- *   The fp32 product is within a few ulps of the correctly rounded one (it
- *   uses expf and one IEEE division), so a code can differ by one step from
- *   a cast of the exactly rounded product.
+ *   Scales: each group's amax is taken from products re-evaluated to about
+ *   2^-44 relative, so scales equal those of the correctly rounded product
+ *   except (rarely) by one fp32 ulp.  Codes: computed from the fp32 product
+ *   (expf and one IEEE division, within a few ulps), so a small fraction of
+ *   codes can differ by one step from a cast of the correctly rounded one.
+ *   gate * up must be finite in fp32 (|gate * up| < 2^128).
  */
 TK_API tk_status tk_swiglu_per_token_cast(const void *x, int64_t M, int64_t N,
                                    int64_t ld_x, int group, int fmt, int mode,

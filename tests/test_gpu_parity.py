@@ -212,6 +212,34 @@ def test_swiglu_small(fmt, mode, layout):
         check_swiglu(case, max_code_frac=2e-3 if M * N < 5000 else 1e-4)
 
 
+def test_swiglu_fp32_scales_track_the_exact_product():
+    """fp32 scales of the fused path: every group's amax element re-evaluated
+    to ~2^-44, so the scale equals the oracle's (correctly rounded product)
+    except within ~2^-44 of a rounding midpoint.  Gates span [-80, 80],
+    with a few beyond (the double-precision fallback)."""
+    M, N, group = 512, 1024, 32
+    rng = np.random.default_rng(21)
+    gate = rng.uniform(-80, 80, size=(M, N)).astype(np.float32)
+    gate[::7] = rng.standard_normal((gate[::7].shape)).astype(np.float32)
+    up = (rng.standard_normal((M, N)) *
+          10.0 ** rng.uniform(-3, 6, size=(M, 1))).astype(np.float32)
+    # row 3: each group's amax element has |gate| > 80 (double fallback);
+    # gate * up stays finite in fp32, as the contract requires
+    gate[3] = rng.standard_normal(N).astype(np.float32) * 0.01
+    up[3] = rng.standard_normal(N).astype(np.float32) * 0.01
+    gate[3, [0, 32, 64, 96]] = [85.0, -90.0, -87.5, 90.0]
+    up[3, [0, 32, 64, 96]] = [2.0, 3e36, 5e35, -3.0]
+    bits = f32_to_bf16_bits(np.concatenate([gate, up], axis=1))
+    case = Case(bits, N, group, "e4m3", "fp32", "row", swiglu=True)
+    gc, gs = case.run_gpu()
+    rc, rs = case.run_oracle()
+    check_swiglu(case, gpu=(gc, gs), ref=(rc, rs), max_code_frac=2e-4)
+    G = N // group
+    sg = gs[1:-1, :G].view(np.int32).astype(np.int64)
+    sr = rs[1:-1, :G].view(np.int32).astype(np.int64)
+    assert np.count_nonzero(sg != sr) <= 2, np.count_nonzero(sg != sr)
+
+
 def test_swiglu_zero_gate_and_strided():
     M, N, group = 33, 256, 64
     bits = random_bf16(8, M, 2 * N)

@@ -1,0 +1,65 @@
+"""The fp32-scale quotient of the CUDA kernel (correctly rounded reciprocal,
+one FMA residual correction -- Markstein's method) equals IEEE division on
+every (x, scale) pair the cast can produce, except where the true quotient
+is below 2^-64 (the residual underflows there); in those cases both values
+encode to the same signed zero (CPU only, exhaustive over about 1.07e9 pairs
+per format).
+
+IEEE fp32 multiply, FMA and division round identically on the host and the
+GPU (no flush to zero on either side), so the host enumeration proves the
+device arithmetic.  The CUDA source is checked to still use that sequence.
+"""
+import os
+import platform
+import re
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(HERE, "quotient_check.c")
+CU = os.path.join(ROOT, "precision_quantization_token_gb300", "csrc",
+                  "tk_cast.cu")
+
+
+def _has_fma_flag():
+    try:
+        return " fma " in open("/proc/cpuinfo").read().replace("\n", " ")
+    except OSError:
+        return False
+
+
+@pytest.fixture(scope="module")
+def checker(tmp_path_factory):
+    exe = str(tmp_path_factory.mktemp("q") / "quotient_check")
+    flags = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math"]
+    if platform.machine() in ("x86_64", "AMD64") and _has_fma_flag():
+        flags.append("-mfma")          # hardware fused multiply-add for fmaf
+    subprocess.run(["gcc", *flags, "-o", exe, SRC, "-lm"], check=True)
+    return exe
+
+
+def test_kernel_uses_the_checked_sequence():
+    """inv = RN(1/s); q0 = x*inv; r = fma(q0, s, -x); q = fma(-r, inv, q0)."""
+    src = open(CU).read()
+    assert re.search(r"g\.inv = __frcp_rn\(r\);", src)
+    body = src[src.index("__device__ __forceinline__ float quotient("):]
+    body = body[:body.index("return q;")]
+    seq = re.findall(r'"(mul\.rn\.f32|neg\.f32|fma\.rn\.f32) ([^;]*);', body)
+    assert seq == [("mul.rn.f32", "q0, %1, %2"), ("neg.f32", "nx, %1"),
+                   ("fma.rn.f32", "r, q0, %3, nx"), ("neg.f32", "r, r"),
+                   ("fma.rn.f32", "%0, r, %2, q0")], seq
+    assert '"f"(x), "f"(g.inv), "f"(g.s)' in body
+
+
+@pytest.mark.parametrize("fmt_max", ["448", "6"])
+def test_every_reachable_pair(checker, fmt_max):
+    out = subprocess.run([checker, fmt_max], check=True, capture_output=True,
+                         text=True, timeout=600)
+    pairs, bad, sub, sub_bad = map(int, out.stdout.split())
+    assert pairs > 10 ** 9
+    assert bad == 0, out.stderr
+    assert sub_bad == 0
+    print(f"{pairs} pairs; {sub} quotients below 2^-64 off by the residual "
+          "underflow, all encoding to the same signed zero")
