@@ -9,10 +9,12 @@ store codes, store scales -- all in one kernel launch) over one batch: the
     python bench.py --impl reference ...     # the CPU oracle as the baseline
 
 Timing: W untimed warm-up steps, then exactly K timed steps between a
-barrier + cuda synchronize on both sides.  Before every step the L2 is
-flushed by writing a buffer of twice its size (outside the timed interval);
-each step's kernel is bracketed by CUDA events on its launching stream, and
-ms_per_step is their mean (max over ranks).  N > 1 runs one independent
+barrier + cuda synchronize on both sides, bracketed by one pair of CUDA
+events on the launching stream; ms_per_step is the mean (max over ranks).
+Inputs are larger than L2: the batch is held in enough copies (at least 3x
+the L2 size together) that each step reads a copy that is not L2-resident.
+A secondary figure times each launch alone between events after an L2
+flush, next to a near-empty kernel timed the same way.  N > 1 runs one independent
 replica of the workload per GPU (rows are independent: no collective on the
 data path), so scaling is weak and value = bytes of all ranks / that time.
 
@@ -50,15 +52,16 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "per_token_cast_c2_traffic.txt"
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=100000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--per-config-steps", type=int, default=2000,
+    ap.add_argument("--per-config-steps", type=int, default=10000,
                     help="timed steps for each of the other workloads "
                          "(0 disables the per-config table)")
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--flush", default="write", choices=["write", "write+read"])
+    ap.add_argument("--flushed-steps", type=int, default=2000,
+                    help="steps of the secondary flushed per-launch timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
@@ -196,60 +199,115 @@ class ClockSampler:
 # ------------------------------------------------------------- GPU arm
 
 class GpuWorkload:
-    """Device buffers for one workload and a launcher through the C ABI."""
+    """Device buffers for one workload and a launcher through the C ABI.
 
-    def __init__(self, w, torch, tk, device):
+    The batch is held in R copies (input and outputs), R chosen so that the
+    copies together are at least 3x the L2 size: step i works on copy i % R,
+    so its input was last touched R-1 steps earlier, with more than twice the
+    L2 size of other traffic in between, and is never L2-resident.  When even
+    32 copies cannot reach that (tiny workloads), R = 1 and the timing
+    flushes the L2 before each step instead.
+    """
+
+    MAX_COPIES = 32
+
+    def __init__(self, w, torch, tk, device, l2_bytes):
         self.w, self.torch, self.tk = w, torch, tk
-        self.bits = make_input(w)
-        self.x = torch.from_numpy(self.bits.view(np.int16)).view(
-            torch.bfloat16).to(device)
+        self.bytes = w.algorithmic_bytes()
+        step = self.bytes["total"]
+        copies = max(1, -(-3 * l2_bytes // step))
+        self.rotating = copies <= self.MAX_COPIES
+        self.copies = copies if self.rotating else 1
+        bits = make_input(w)
+        x0 = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
         row_bytes = w.K if w.fmt == "e4m3" else w.K // 2
-        self.codes = torch.empty((w.M, row_bytes), dtype=torch.uint8,
-                                 device=device)
         shape, dt = tk.scale_shape(w.M, w.K, w.group, w.scale, w.layout)
-        self.scales = torch.empty(shape, dtype=getattr(torch, dt),
-                                  device=device)
+        self.sets = []
+        for i in range(self.copies):
+            x = x0 if i == 0 else x0.clone()
+            codes = torch.empty((w.M, row_bytes), dtype=torch.uint8, device=device)
+            scales = torch.empty(shape, dtype=getattr(torch, dt), device=device)
+            self.sets.append((x, codes, scales))
         self.entry = (tk.tk_swiglu_per_token_cast if w.swiglu
                       else tk.tk_per_token_cast)
-        self.bytes = w.algorithmic_bytes()
 
-    def launch(self, stream_handle):
+    def launch(self, i, stream_handle):
         w, tk = self.w, self.tk
-        self.entry(self.x.data_ptr(), w.M, w.K, self.x.stride(0), w.group,
+        x, codes, scales = self.sets[i % self.copies]
+        self.entry(x.data_ptr(), w.M, w.K, x.stride(0), w.group,
                    tk.FMT[w.fmt], tk.SCALE[w.scale], tk.LAYOUT[w.layout],
-                   self.codes.data_ptr(), self.codes.stride(0),
-                   self.scales.data_ptr(), self.scales.stride(0),
-                   stream_handle)
+                   codes.data_ptr(), codes.stride(0), scales.data_ptr(),
+                   scales.stride(0), stream_handle)
+
+    def l2_note(self, l2_bytes):
+        if self.rotating:
+            mib = self.copies * self.bytes["total"] / 2 ** 20
+            return (f"inputs larger than L2: {self.copies} copies of the batch "
+                    f"({mib:.0f} MiB of inputs+outputs, L2 {l2_bytes >> 20} "
+                    "MiB) cycled step by step, no step's input L2-resident")
+        return (f"L2 flushed before every step by writing {2 * l2_bytes >> 20}"
+                f" MiB then reading {l2_bytes >> 20} MiB (outside the timed "
+                "events)")
 
 
-def time_steps(torch, wl, steps, warmup, flush_buf, flush_read, world):
-    """Per-step kernel times (ms) with the L2 flushed before each step."""
+def _flush(torch, fw, fr):
+    fw.zero_()
+    fr.sum(dtype=torch.float32)
+
+
+def time_steps(torch, wl, steps, warmup, fw, fr, world):
+    """Mean ms per step over exactly `steps` steps, events on the launching
+    stream; returns (mean ms, wall seconds of the timed region)."""
     stream = torch.cuda.current_stream()
     handle = stream.cuda_stream
-
-    def flush():
-        flush_buf.zero_()
-        if flush_read is not None:
-            flush_read.sum(dtype=torch.float32)
-
-    for _ in range(warmup):
-        flush()
-        wl.launch(handle)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(warmup):
+        if not wl.rotating:
+            _flush(torch, fw, fr)
+        wl.launch(i, handle)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for i in range(steps):
-        flush()
-        starts[i].record(stream)
-        wl.launch(handle)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    if wl.rotating:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            wl.launch(warmup + i, handle)
+        b.record(stream)
+        torch.cuda.synchronize()
+        total = a.elapsed_time(b)
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i, (a, b) in enumerate(ev):
+            _flush(torch, fw, fr)
+            a.record(stream)
+            wl.launch(warmup + i, handle)
+            b.record(stream)
+        torch.cuda.synchronize()
+        total = sum(a.elapsed_time(b) for a, b in ev)
     barrier(world)
-    wall = time.perf_counter() - t0
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return ms, wall
+    return total / steps, time.perf_counter() - t0
+
+
+def time_flushed(torch, wl, steps, fw, fr, launch=None):
+    """Secondary figure: each launch alone between CUDA events, with the L2
+    flushed (2x L2 written, then L2 read) before it."""
+    stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream
+    launch = launch or (lambda i: wl.launch(i, handle))
+    for i in range(5):
+        _flush(torch, fw, fr)
+        launch(i)
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (a, b) in enumerate(ev):
+        _flush(torch, fw, fr)
+        a.record(stream)
+        launch(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.fmean(a.elapsed_time(b) for a, b in ev)
 
 
 def run_gpu(args):
@@ -265,21 +323,19 @@ def run_gpu(args):
     tk.load()
 
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
-    flush_read = (torch.ones(2 * l2 // 2, dtype=torch.bfloat16, device=device)
-                  if args.flush == "write+read" else None)
+    fw = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    fr = torch.ones(l2 // 2, dtype=torch.bfloat16, device=device)
 
     w = WORKLOADS[args.workload]
-    wl = GpuWorkload(w, torch, tk, device)
+    wl = GpuWorkload(w, torch, tk, device, l2)
     peak, peak_src = measured_peaks()
 
     clocks = ClockSampler(local_rank)
     clocks.start()
-    ms, wall = time_steps(torch, wl, args.steps, args.warmup, flush_buf,
-                          flush_read, world)
+    mean_ms, wall = time_steps(torch, wl, args.steps, args.warmup, fw, fr,
+                               world)
     clock_info = clocks.stop()
 
-    mean_ms = statistics.fmean(ms)
     mean_ms_all = reduce_max(mean_ms, world)
     total_bytes = wl.bytes["total"] * world
     value = total_bytes / (mean_ms_all * 1e-3) / 1e9
@@ -295,14 +351,10 @@ def run_gpu(args):
             "workload": w.describe(), "name": w.name, "M": w.M, "K": w.K,
             "group": w.group, "fmt": w.fmt, "scale": w.scale,
             "layout": w.layout, "swiglu": w.swiglu, "seed": w.seed,
-            "bytes_per_step": wl.bytes,
-            "l2": f"flushed before every step by writing {2 * l2 >> 20} MiB"
-                  + (" then reading 2x L2" if flush_read is not None else "")
-                  + " (outside the timed events)",
-            "timing": "CUDA events around each launch on its stream; mean "
-                      "of the steps; max over ranks",
-            "median_ms": round(statistics.median(ms), 6),
-            "min_ms": round(min(ms), 6),
+            "bytes_per_step": wl.bytes, "l2": wl.l2_note(l2),
+            "timing": ("one CUDA event pair on the launching stream around "
+                       "exactly K back-to-back steps (one kernel launch "
+                       "each); mean per step; max over ranks"),
             "wall_s_timed_region": round(wall, 3),
             "parallelism": f"replicas x{world} (rows independent)"},
         "roofline": {
@@ -314,21 +366,34 @@ def run_gpu(args):
         "clocks": clock_info,
     }
 
+    if rank == 0 and args.flushed_steps > 0:
+        f_ms = time_flushed(torch, wl, args.flushed_steps, fw, fr)
+        e_ms = time_flushed(torch, wl, args.flushed_steps, fw, fr,
+                            launch=lambda i: torch.cuda._sleep(1))
+        result["flushed_per_launch"] = {
+            "ms": round(f_ms, 6),
+            "GB/s": round(wl.bytes["total"] / f_ms / 1e6, 1),
+            "frac_of_peak": round(wl.bytes["total"] / f_ms / 1e6 / peak, 4),
+            "empty_kernel_ms": round(e_ms, 6),
+            "how": ("each launch alone between CUDA events after an L2 flush "
+                    "(2x L2 written then L2 read); empty_kernel_ms is a "
+                    "near-empty kernel timed the same way (event and launch "
+                    "overhead included in both)")}
+
     if rank == 0 and args.per_config_steps > 0:
         table = {}
         for name in sorted(WORKLOADS):
             if name == w.name:
                 continue
-            other = GpuWorkload(WORKLOADS[name], torch, tk, device)
-            oms, _ = time_steps(torch, other, args.per_config_steps,
-                                max(3, args.warmup // 5), flush_buf,
-                                flush_read, 1)
-            m = statistics.fmean(oms)
+            other = GpuWorkload(WORKLOADS[name], torch, tk, device, l2)
+            m, _ = time_steps(torch, other, args.per_config_steps,
+                              max(3, args.warmup), fw, fr, 1)
             gbps = other.bytes["total"] / (m * 1e-3) / 1e9
             table[name] = {"workload": other.w.describe(),
                            "ms": round(m, 6), "GB/s": round(gbps, 1),
                            "frac_of_peak": round(gbps / peak, 4),
-                           "bytes": other.bytes["total"]}
+                           "bytes": other.bytes["total"],
+                           "l2": other.l2_note(l2)}
             del other
         result["per_config"] = table
 

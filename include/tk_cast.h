@@ -128,6 +128,18 @@ TK_API tk_status tk_swiglu_per_token_cast(const void *x, int64_t M, int64_t N,
                                    void *scales, int64_t ld_scales,
                                    void *stream);
 
+/*
+ * tk_get_device_fault -- read (and optionally clear) the library's device
+ * fault word on the current device.  Every wait inside the kernels is
+ * bounded in time (1 s); a wait that runs out makes the kernel stop, let its
+ * own in-flight copies land and return, OR-ing a code into this word:
+ *   1 = a consumer waited too long for a tile, 2 = the producer waited too
+ *   long for a free stage, 4 = in-flight copies did not land in time.
+ * 0 means no kernel has given up.  Synchronous (device-to-host copy of one
+ * word); TK_ERR_INVALID_ARG for a null pointer, TK_ERR_CUDA if the copy fails.
+ */
+TK_API tk_status tk_get_device_fault(unsigned int *fault, int clear);
+
 /* Static string naming a status value ("TK_OK", ...). */
 TK_API const char *tk_status_string(int status);
 

@@ -77,6 +77,8 @@ def load():
                 fn = getattr(lib, name)
                 fn.argtypes = sig
                 fn.restype = i
+            lib.tk_get_device_fault.argtypes = [p, i]
+            lib.tk_get_device_fault.restype = i
             lib.tk_status_string.argtypes = [i]
             lib.tk_status_string.restype = ctypes.c_char_p
             lib.tk_last_cuda_error.argtypes = []
@@ -110,6 +112,14 @@ def tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, group, fmt, mode, layout,
     _check(load().tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, group, fmt,
                                            mode, layout, codes_ptr, ld_codes,
                                            scales_ptr, ld_scales, stream))
+
+
+def tk_get_device_fault(clear: bool = False) -> int:
+    """The device fault word of the current device (0: no kernel gave up on
+    a wait); see include/tk_cast.h."""
+    word = ctypes.c_uint(0)
+    _check(load().tk_get_device_fault(ctypes.byref(word), int(clear)))
+    return word.value
 
 
 def tk_status_string(status: int) -> str:

@@ -22,6 +22,7 @@ NVCC_FLAGS = [
     ARCH, "-O3", "-lineinfo", "-std=c++17",
     "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-fmad=false",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+    "-Xcompiler", "-Wall", "-Xcompiler", "-Wextra",
     "-shared", f"-I{INCLUDE}",
 ]
 

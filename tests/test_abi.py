@@ -97,6 +97,10 @@ def test_empty_batch_is_a_noop(lib):
                 ld_x=512) == OK
 
 
+def test_fault_query_rejects_null(lib):
+    assert lib.tk_get_device_fault(None, 0) == INVALID
+
+
 def test_python_wrapper_raises(lib):
     with pytest.raises(tk.TkError) as e:
         tk.tk_per_token_cast(A, 4, 256, 256, 48, 0, 0, 0, B, 256, C, 2, 0)

@@ -285,3 +285,8 @@ def test_bf16_input_values_roundtrip():
         np.repeat(scales.cpu().numpy(), 128, axis=1)
     xf = bf16_bits_to_f32(bits)
     assert np.max(np.abs(deq - xf)) <= np.max(np.abs(xf)) / 16
+
+
+def test_zz_no_kernel_gave_up_on_a_wait():
+    """No kernel of this module's runs hit its bounded-wait limit."""
+    assert tk.tk_get_device_fault(clear=True) == 0
