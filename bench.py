@@ -86,6 +86,14 @@ def reduce_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+def job_throughput(bytes_per_step: int, mean_ms: float, world: int):
+    """(whole-job GB/s, slowest rank's ms per step): every rank processes
+    its own replica of the workload (weak scaling), so the job moves
+    world x bytes_per_step per step in the slowest rank's time."""
+    slowest = reduce_max(mean_ms, world)
+    return bytes_per_step * world / (slowest * 1e-3) / 1e9, slowest
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -336,9 +344,7 @@ def run_gpu(args):
                                world)
     clock_info = clocks.stop()
 
-    mean_ms_all = reduce_max(mean_ms, world)
-    total_bytes = wl.bytes["total"] * world
-    value = total_bytes / (mean_ms_all * 1e-3) / 1e9
+    value, mean_ms_all = job_throughput(wl.bytes["total"], mean_ms, world)
     achieved = wl.bytes["total"] / (mean_ms * 1e-3) / 1e9
 
     result = {
