@@ -72,6 +72,12 @@ def _configure(lib):
     lib.oracle_scale.restype = None
     lib.oracle_swiglu_values.argtypes = [p, i64, i64, i64, i64, p, i64]
     lib.oracle_swiglu_values.restype = None
+    lib.oracle_per_token_dequant.argtypes = [p, i64, p, i64, i64, i64, i64, i,
+                                             i, i, i, i, p, i64]
+    lib.oracle_per_token_dequant.restype = i
+    lib.oracle_per_token_cast_back.argtypes = [p, i64, i64, i64, i64, i, i, i,
+                                               p, i64]
+    lib.oracle_per_token_cast_back.restype = i
     return lib
 
 
@@ -212,6 +218,56 @@ def swiglu_values(x_bits: np.ndarray, N: int, threads: int = 1) -> np.ndarray:
         work(0)
     else:
         list(_executor(threads).map(work, range(threads)))
+    return y
+
+
+def _split(n_rows, threads, work):
+    threads = max(1, min(threads or 1, n_rows)) if n_rows else 1
+    bounds = np.linspace(0, n_rows, threads + 1).astype(np.int64)
+    jobs = [(int(bounds[t]), int(bounds[t + 1])) for t in range(threads)]
+    if threads == 1:
+        rcs = [work(*jobs[0])]
+    else:
+        rcs = list(_executor(threads).map(lambda j: work(*j), jobs))
+    for rc in rcs:
+        if rc != 0:
+            raise ValueError(f"oracle returned status {rc}")
+
+
+def per_token_dequant(codes: np.ndarray, scales: np.ndarray, K: int,
+                      group: int, fmt: int, mode: int, layout: int, *,
+                      out_fp32: bool = False, threads: int = 1):
+    """Oracle dequantization: code value x scale (one fp32 multiply), as
+    fp32 or rounded to BF16 bits.  codes/scales as the cast writes them."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales)
+    M = codes.shape[0]
+    y = np.zeros((M, K), np.float32 if out_fp32 else np.uint16)
+    lib = _load()
+    ld_s = scales.strides[0] // scales.itemsize
+
+    def work(a, b):
+        return lib.oracle_per_token_dequant(
+            _ptr(codes), codes.strides[0], _ptr(scales), ld_s, a, b, K,
+            group, fmt, mode, layout, int(out_fp32), _ptr(y), K)
+
+    _split(M, threads, work)
+    return y
+
+
+def per_token_cast_back(x_bits: np.ndarray, K: int, group: int, fmt: int,
+                        mode: int, *, threads: int = 1) -> np.ndarray:
+    """Oracle cast-and-cast-back: BF16 bits in, BF16 bits out."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, ld_x = x_bits.shape
+    y = np.zeros((M, K), np.uint16)
+    lib = _load()
+
+    def work(a, b):
+        return lib.oracle_per_token_cast_back(_ptr(x_bits), a, b, K, ld_x,
+                                              group, fmt, mode, _ptr(y), K)
+
+    _split(M, threads, work)
     return y
 
 

@@ -359,6 +359,144 @@ void oracle_swiglu_values(const uint16_t *x, int64_t m_begin, int64_t m_end,
     }
 }
 
+/* ------------------------------------------------ dequantization (decode) */
+
+/*
+ * Value of an E4M3FN code (OCP 8-bit floating point): sign | exponent e
+ * (bias 7) | mantissa m (3 bits); e == 0 is subnormal, m * 2^-9.  The NaN
+ * pattern S.1111.111 is never produced by the cast; it decodes to NaN.
+ */
+static float e4m3_decode(uint8_t c)
+{
+    int e = (c >> 3) & 0xF, m = c & 7;
+    float mag;
+    if (e == 15 && m == 7)
+        mag = NAN;
+    else if (e == 0)
+        mag = ldexpf((float)m, -9);
+    else
+        mag = ldexpf(1.0f + (float)m / 8.0f, e - 7);
+    return (c & 0x80) ? -mag : mag;
+}
+
+/* Value of an E2M1 code (OCP MX): sign | exponent e (bias 1) | mantissa m
+ * (1 bit); e == 0 is subnormal, m * 0.5. */
+static float e2m1_decode(uint8_t c)
+{
+    int e = (c >> 1) & 3, m = c & 1;
+    float mag = e == 0 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
+    return (c & 0x8) ? -mag : mag;
+}
+
+/* fp32 -> BF16 bits, round to nearest, ties to even (NaN kept quiet). */
+static uint16_t float_to_bf16_bits(float f)
+{
+    uint32_t u = float_bits(f);
+    if (isnan(f))
+        return (uint16_t)((u >> 16) | 0x40);
+    uint32_t lower = u & 0xFFFFu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1;                       /* carries into the exponent too */
+    return (uint16_t)upper;
+}
+
+/* Scale of group j of row m read back from a scale tensor written by the
+ * cast (fp32 value, or 2^(byte-127) for packed UE8M0). */
+static float read_scale(const void *scales, int64_t ld_scales, int mode,
+                        int layout, int64_t m, int64_t j)
+{
+    if (mode == OR_SCALE_UE8M0) {
+        const uint8_t *base = (const uint8_t *)scales;
+        int64_t w = j / 4, b = j % 4;
+        int64_t word = layout == OR_LAYOUT_ROW_MAJOR ? m * ld_scales + w
+                                                     : w * ld_scales + m;
+        return ldexpf(1.0f, (int)base[word * 4 + b] - 127);
+    }
+    const float *base = (const float *)scales;
+    return layout == OR_LAYOUT_ROW_MAJOR ? base[m * ld_scales + j]
+                                         : base[j * ld_scales + m];
+}
+
+/*
+ * Per-token dequantization of rows [m_begin, m_end): y = code value * scale,
+ * one fp32 multiply per element, written as fp32 (out_fp32 != 0) or rounded
+ * to BF16 (nearest even).  codes/scales are laid out as the cast writes them.
+ * y row m at y + m * ld_y (elements of the output type).
+ */
+int oracle_per_token_dequant(const uint8_t *codes, int64_t ld_codes,
+                             const void *scales, int64_t ld_scales,
+                             int64_t m_begin, int64_t m_end, int64_t K,
+                             int group, int fmt, int mode, int layout,
+                             int out_fp32, void *y, int64_t ld_y)
+{
+    int rc = check_common(K, group, fmt, mode, layout);
+    if (rc != OR_OK)
+        return rc;
+    for (int64_t m = m_begin; m < m_end; ++m) {
+        const uint8_t *cr = codes + m * ld_codes;
+        for (int64_t k = 0; k < K; ++k) {
+            float v;
+            if (fmt == OR_FMT_E4M3) {
+                v = e4m3_decode(cr[k]);
+            } else {
+                uint8_t byte = cr[k / 2];
+                v = e2m1_decode((uint8_t)((k & 1) ? byte >> 4 : byte & 0xF));
+            }
+            float s = read_scale(scales, ld_scales, mode, layout, m, k / group);
+            float prod = v * s;
+            if (out_fp32)
+                ((float *)y)[m * ld_y + k] = prod;
+            else
+                ((uint16_t *)y)[m * ld_y + k] = float_to_bf16_bits(prod);
+        }
+    }
+    return OR_OK;
+}
+
+/*
+ * Per-token cast-and-cast-back (quantisation round trip) of rows
+ * [m_begin, m_end): each row is cast exactly as oracle_per_token_cast casts
+ * it, then dequantized as oracle_per_token_dequant does, into BF16 y.
+ */
+int oracle_per_token_cast_back(const uint16_t *x, int64_t m_begin,
+                               int64_t m_end, int64_t K, int64_t ld_x,
+                               int group, int fmt, int mode, uint16_t *y,
+                               int64_t ld_y)
+{
+    int rc = check_common(K, group, fmt, mode, OR_LAYOUT_ROW_MAJOR);
+    if (rc != OR_OK)
+        return rc;
+    int64_t G = K / group;
+    int64_t words = mode == OR_SCALE_UE8M0 ? (G + 3) / 4 : G;
+    float *row = (float *)malloc((size_t)K * sizeof(float));
+    uint8_t *codes = (uint8_t *)calloc((size_t)K, 1);
+    uint32_t *sc = (uint32_t *)calloc((size_t)words, sizeof(uint32_t));
+    if (!row || !codes || !sc) {
+        free(row);
+        free(codes);
+        free(sc);
+        return OR_BAD_ARG;
+    }
+    for (int64_t m = m_begin; m < m_end && rc == OR_OK; ++m) {
+        const uint16_t *xr = x + m * ld_x;
+        for (int64_t k = 0; k < K; ++k)
+            row[k] = bf16_bits_to_float(xr[k]);
+        /* one-row scratch: row index 0, row-major scales */
+        rc = cast_row(row, K, group, fmt, mode, OR_LAYOUT_ROW_MAJOR, 0, codes,
+                      sc, words);
+        if (rc == OR_OK)
+            rc = oracle_per_token_dequant(codes, 0, sc, words, 0, 1, K,
+                                          group, fmt, mode,
+                                          OR_LAYOUT_ROW_MAJOR, 0,
+                                          y + m * ld_y, 0);
+    }
+    free(row);
+    free(codes);
+    free(sc);
+    return rc;
+}
+
 /* ------------------------------------------- element-level hooks for pins */
 
 /* Saturating RNE encode of n fp32 values (the code step of the cast alone). */

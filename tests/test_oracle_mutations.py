@@ -13,6 +13,7 @@ import pytest
 import oracle
 import test_oracle_cast as tc
 import test_oracle_codec as tk
+import test_oracle_dequant as td
 import test_oracle_scale as ts
 import test_oracle_swiglu as tw
 
@@ -44,12 +45,22 @@ MUTATIONS = {
     "scale_multiplied": ("float q = yg[k] / sc.s;", "float q = yg[k] * sc.s;"),
     "amax_without_abs": ("float a = fabsf(yg[k]);", "float a = yg[k];"),
     "saturation_dropped": ("if (a > 448.0f)\n        a = 448.0f;", ""),
+    "decode_bias": ("mag = ldexpf(1.0f + (float)m / 8.0f, e - 7);",
+                    "mag = ldexpf(1.0f + (float)m / 8.0f, e - 8);"),
+    "decode_subnormal_step": ("mag = ldexpf((float)m, -9);",
+                              "mag = ldexpf((float)m, -10);"),
+    "decode_e2m1_subnormal": ("e == 0 ? 0.5f * (float)m", "e == 0 ? 1.0f * (float)m"),
+    "bf16_ties_up": ("(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
+    "bf16_truncates": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))\n        upper += 1;", ""),
+    "dequant_nibble_order": ("(k & 1) ? byte >> 4 : byte & 0xF", "(k & 1) ? byte & 0xF : byte >> 4"),
+    "dequant_scale_transposed_index": ("                                         : base[j * ld_scales + m];",
+                                       "                                         : base[m * 0 + j * ld_scales];"),
 }
 
 
 def _pin_functions():
     fns = []
-    for mod in (tk, ts, tc, tw):
+    for mod in (tk, ts, tc, tw, td):
         for name, fn in inspect.getmembers(mod, inspect.isfunction):
             if name.startswith("test_") and fn.__module__ == mod.__name__:
                 fns.append(fn)
