@@ -230,9 +230,24 @@ class GpuWorkload:
         x0 = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
         row_bytes = w.K if w.fmt == "e4m3" else w.K // 2
         shape, dt = tk.scale_shape(w.M, w.K, w.group, w.scale, w.layout)
+        if w.op == "dequant":
+            # the codes and scales to dequantize come from one (untimed) cast
+            c0, s0 = tk.per_token_cast(x0, w.group, w.fmt, w.scale, w.layout)
+            torch.cuda.synchronize()
+            del x0
         self.sets = []
         for i in range(self.copies):
+            if w.op == "dequant":
+                codes = c0 if i == 0 else c0.clone()
+                scales = s0 if i == 0 else s0.clone()
+                y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device)
+                self.sets.append((codes, scales, y))
+                continue
             x = x0 if i == 0 else x0.clone()
+            if w.op == "cast_back":
+                y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device)
+                self.sets.append((x, y, None))
+                continue
             codes = torch.empty((w.M, row_bytes), dtype=torch.uint8, device=device)
             scales = torch.empty(shape, dtype=getattr(torch, dt), device=device)
             self.sets.append((x, codes, scales))
@@ -241,11 +256,24 @@ class GpuWorkload:
 
     def launch(self, i, stream_handle):
         w, tk = self.w, self.tk
-        x, codes, scales = self.sets[i % self.copies]
-        self.entry(x.data_ptr(), w.M, w.K, x.stride(0), w.group,
-                   tk.FMT[w.fmt], tk.SCALE[w.scale], tk.LAYOUT[w.layout],
-                   codes.data_ptr(), codes.stride(0), scales.data_ptr(),
-                   scales.stride(0), stream_handle)
+        a, b, c = self.sets[i % self.copies]
+        if w.op == "dequant":
+            tk.tk_per_token_dequant(a.data_ptr(), a.stride(0), b.data_ptr(),
+                                    b.stride(0), w.M, w.K, w.group,
+                                    tk.FMT[w.fmt], tk.SCALE[w.scale],
+                                    tk.LAYOUT[w.layout], c.data_ptr(),
+                                    c.stride(0), tk.OUT_DTYPE["bf16"],
+                                    stream_handle)
+        elif w.op == "cast_back":
+            tk.tk_per_token_cast_back(a.data_ptr(), w.M, w.K, a.stride(0),
+                                      w.group, tk.FMT[w.fmt],
+                                      tk.SCALE[w.scale], b.data_ptr(),
+                                      b.stride(0), stream_handle)
+        else:
+            self.entry(a.data_ptr(), w.M, w.K, a.stride(0), w.group,
+                       tk.FMT[w.fmt], tk.SCALE[w.scale], tk.LAYOUT[w.layout],
+                       b.data_ptr(), b.stride(0), c.data_ptr(), c.stride(0),
+                       stream_handle)
 
     def l2_note(self, l2_bytes):
         if self.rotating:

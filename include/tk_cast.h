@@ -87,6 +87,11 @@ typedef enum {
     TK_SCALE_TRANSPOSED_PADDED = 1
 } tk_scale_layout;
 
+typedef enum {
+    TK_OUT_BF16 = 0,  /* dequantized values rounded to BF16 (nearest even) */
+    TK_OUT_FP32 = 1   /* dequantized values as fp32 */
+} tk_out_dtype;
+
 /*
  * tk_per_token_cast -- per-token group-wise cast of a BF16 matrix.
  *
@@ -127,6 +132,50 @@ TK_API tk_status tk_swiglu_per_token_cast(const void *x, int64_t M, int64_t N,
                                    int layout, void *codes, int64_t ld_codes,
                                    void *scales, int64_t ld_scales,
                                    void *stream);
+
+/*
+ * tk_per_token_dequant -- per-token dequantization (TileKernels README,
+ * "Features": "FP8/FP4 casting and dequantization"): the inverse of the cast.
+ *
+ *   y[m, k] = value(code[m, k]) * scale(m, k / group)
+ *   one IEEE fp32 multiply; value() decodes E4M3FN / E2M1 exactly; the scale
+ *   is read from a tensor laid out as tk_per_token_cast writes it (fp32, or
+ *   packed UE8M0 byte e giving 2^(e-127)).  Output fp32, or rounded to BF16
+ *   with round-to-nearest-even (out_dtype, tk_out_dtype).
+ *
+ *   codes     uint8 [M][ld_codes] (K or K/2 bytes used per row), 16-byte
+ *             aligned, ld_codes a multiple of 16.  For E2M1 with K not a
+ *             multiple of 32, the kernel reads each row up to the next
+ *             16-byte boundary: the buffer must span M * ld_codes bytes.
+ *   scales    as for tk_per_token_cast with the same mode/layout/ld_scales.
+ *   y         [M][ld_y] elements of out_dtype, 16-byte aligned,
+ *             ld_y * sizeof(element) a multiple of 16, ld_y >= K.
+ *   Codes that the cast never writes still decode: the E4M3 NaN pattern
+ *   gives NaN, and a product beyond the output range gives +-inf.
+ */
+TK_API tk_status tk_per_token_dequant(const void *codes, int64_t ld_codes,
+                                      const void *scales, int64_t ld_scales,
+                                      int64_t M, int64_t K, int group, int fmt,
+                                      int mode, int layout, void *y,
+                                      int64_t ld_y, int out_dtype,
+                                      void *stream);
+
+/*
+ * tk_per_token_cast_back -- per-token cast-and-cast-back (aiwiki
+ * "TileKernels", section "Version 2.0.0": "per-token cast-and-cast-back"):
+ * each row is cast exactly as tk_per_token_cast casts it, and the codes are
+ * dequantized again in the same pass (as tk_per_token_dequant with BF16
+ * output), so y holds the BF16 values the quantized tensor represents.
+ * Neither codes nor scales are written.
+ *
+ *   x    BF16 [M][ld_x] as for tk_per_token_cast.
+ *   y    BF16 [M][ld_y], 16-byte aligned, ld_y * 2 a multiple of 16, ld_y >= K.
+ *   group, fmt, mode: as for tk_per_token_cast (no scale layout: no scales).
+ */
+TK_API tk_status tk_per_token_cast_back(const void *x, int64_t M, int64_t K,
+                                        int64_t ld_x, int group, int fmt,
+                                        int mode, void *y, int64_t ld_y,
+                                        void *stream);
 
 /*
  * tk_get_device_fault -- read (and optionally clear) the library's device

@@ -10,11 +10,17 @@ Low level (same names and arguments as the C ABI, raw pointers and sizes):
     tk_per_token_cast(x_ptr, M, K, ld_x, group, fmt, mode, layout,
                       codes_ptr, ld_codes, scales_ptr, ld_scales, stream)
     tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, ...)
+    tk_per_token_dequant(codes_ptr, ld_codes, scales_ptr, ld_scales, M, K,
+                         group, fmt, mode, layout, y_ptr, ld_y, out_dtype, stream)
+    tk_per_token_cast_back(x_ptr, M, K, ld_x, group, fmt, mode, y_ptr, ld_y,
+                           stream)
 
 Tensor level (allocates outputs with torch):
     codes, scales = per_token_cast(x, group=128, fmt="e4m3", scale="fp32",
                                    layout="row")
     codes, scales = swiglu_per_token_cast(x, group=128, ...)  # x = [gate|up]
+    y = per_token_dequant(codes, scales, K, group=128, fmt="e4m3", ...)
+    y = per_token_cast_back(x, group=128, fmt="e4m3", scale="fp32")
 
 Operation (TileKernels README, "Features"; aiwiki "TileKernels", section
 "Quantization"): per row and per group of 16/32/64/128 channels, amax, a
@@ -31,6 +37,7 @@ import threading
 from . import _build
 
 FMT = {"e4m3": 0, "e2m1": 1}
+OUT_DTYPE = {"bf16": 0, "fp32": 1}
 SCALE = {"fp32": 0, "pow2": 1, "ue8m0": 2}
 LAYOUT = {"row": 0, "transposed": 1}
 
@@ -77,6 +84,12 @@ def load():
                 fn = getattr(lib, name)
                 fn.argtypes = sig
                 fn.restype = i
+            lib.tk_per_token_cast_back.argtypes = [p, i64, i64, i64, i, i, i,
+                                                   p, i64, p]
+            lib.tk_per_token_cast_back.restype = i
+            lib.tk_per_token_dequant.argtypes = [p, i64, p, i64, i64, i64, i, i,
+                                                 i, i, p, i64, i, p]
+            lib.tk_per_token_dequant.restype = i
             lib.tk_get_device_fault.argtypes = [p, i]
             lib.tk_get_device_fault.restype = i
             lib.tk_status_string.argtypes = [i]
@@ -112,6 +125,22 @@ def tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, group, fmt, mode, layout,
     _check(load().tk_swiglu_per_token_cast(x_ptr, M, N, ld_x, group, fmt,
                                            mode, layout, codes_ptr, ld_codes,
                                            scales_ptr, ld_scales, stream))
+
+
+def tk_per_token_cast_back(x_ptr, M, K, ld_x, group, fmt, mode, y_ptr, ld_y,
+                           stream=0) -> None:
+    """Raw-pointer call of the cast-and-cast-back entry point."""
+    _check(load().tk_per_token_cast_back(x_ptr, M, K, ld_x, group, fmt, mode,
+                                         y_ptr, ld_y, stream))
+
+
+def tk_per_token_dequant(codes_ptr, ld_codes, scales_ptr, ld_scales, M, K,
+                         group, fmt, mode, layout, y_ptr, ld_y, out_dtype,
+                         stream=0) -> None:
+    """Raw-pointer call of the dequantization entry point."""
+    _check(load().tk_per_token_dequant(codes_ptr, ld_codes, scales_ptr,
+                                       ld_scales, M, K, group, fmt, mode,
+                                       layout, y_ptr, ld_y, out_dtype, stream))
 
 
 def tk_get_device_fault(clear: bool = False) -> int:
@@ -205,3 +234,41 @@ def swiglu_per_token_cast(x, group: int = 128, fmt: str = "e4m3",
     N = x.shape[1] // 2
     return _call(tk_swiglu_per_token_cast, x, N, group, fmt, scale, layout,
                  codes, scales, stream)
+
+
+def per_token_dequant(codes, scales, K: int, group: int = 128,
+                      fmt: str = "e4m3", scale: str = "fp32",
+                      layout: str = "row", out_dtype: str = "bf16", *,
+                      out=None, stream=None):
+    """Dequantize codes [M, K or K/2] (uint8, CUDA) with their scales (as
+    per_token_cast returns them): code value x scale, BF16 or fp32 [M, K]."""
+    import torch
+    M = codes.shape[0]
+    if out is None:
+        dt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+        out = torch.empty((M, K), dtype=dt, device=codes.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(codes.device).cuda_stream
+    tk_per_token_dequant(codes.data_ptr(), codes.stride(0), scales.data_ptr(),
+                         scales.stride(0), M, K, group, FMT[fmt], SCALE[scale],
+                         LAYOUT[layout], out.data_ptr(), out.stride(0),
+                         OUT_DTYPE[out_dtype], stream)
+    return out
+
+
+def per_token_cast_back(x, group: int = 128, fmt: str = "e4m3",
+                        scale: str = "fp32", *, out=None, stream=None):
+    """Quantize then dequantize a bfloat16 [M, K] CUDA tensor in one pass:
+    the BF16 values its per-token cast represents."""
+    import torch
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D bfloat16 tensor with unit column "
+                         "stride")
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    tk_per_token_cast_back(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt],
+                           SCALE[scale], out.data_ptr(), out.stride(0), stream)
+    return out

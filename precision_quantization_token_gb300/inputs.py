@@ -17,6 +17,8 @@ Workloads are the shapes and value mixes the per-token cast is measured on:
   c5   E2M1, 32768 x 7168, group 16, UE8M0 packed; N(0,1) with a seeded 1%
        of rows all +0 and a disjoint 1% of rows of BF16 denormals (exponent
        field 0, mantissa uniform in 1..127, random sign)
+  d2   dequantization of c2's codes and scales to BF16 (4096 x 7168)
+  b2   cast-and-cast-back of c2's input (4096 x 7168, E4M3 g128 UE8M0)
 
 Random draws use numpy's PCG64 generator seeded per workload; fp32 values are
 rounded to BF16 with round-to-nearest-even on the bit pattern.
@@ -42,6 +44,7 @@ class Workload:
     swiglu: bool
     seed: int
     dist: str
+    op: str = "cast"   # "cast" | "swiglu" | "dequant" | "cast_back"
 
     @property
     def in_cols(self) -> int:
@@ -53,17 +56,26 @@ class Workload:
 
     def algorithmic_bytes(self) -> dict:
         """Bytes read once and written once (padding not counted)."""
-        read = self.M * self.in_cols * 2
         codes = self.M * self.K if self.fmt == "e4m3" else self.M * self.K // 2
         if self.scale == "ue8m0":
             scales = self.M * ((self.groups + 3) // 4) * 4
         else:
             scales = self.M * self.groups * 4
+        if self.op == "dequant":
+            out = self.M * self.K * 2
+            return {"read": codes + scales, "bf16_out": out,
+                    "total": codes + scales + out}
+        if self.op == "cast_back":
+            read = self.M * self.K * 2
+            return {"read": read, "bf16_out": read, "total": 2 * read}
+        read = self.M * self.in_cols * 2
         return {"read": read, "codes": codes, "scales": scales,
                 "total": read + codes + scales}
 
     def describe(self) -> str:
-        op = "swiglu_per_token_cast" if self.swiglu else "per_token_cast"
+        op = {"cast": "per_token_cast", "swiglu": "swiglu_per_token_cast",
+              "dequant": "per_token_dequant",
+              "cast_back": "per_token_cast_back"}[self.op]
         shape = (f"{self.M}x{self.in_cols}->{self.M}x{self.K}" if self.swiglu
                  else f"{self.M}x{self.K}")
         return (f"{op} {self.fmt.upper()} g{self.group} {self.scale} "
@@ -80,9 +92,13 @@ WORKLOADS = {
     "c3b": Workload("c3b", 16384, 4096, 64, "e4m3", "fp32", "transposed",
                     False, 3, "normal x U(0.01,10) per row"),
     "c4": Workload("c4", 8192, 2048, 128, "e4m3", "ue8m0", "row", True, 4,
-                   "normal"),
+                   "normal", op="swiglu"),
     "c5": Workload("c5", 32768, 7168, 16, "e2m1", "ue8m0", "row", False, 5,
                    "normal, 1% zero rows, 1% denormal rows"),
+    "d2": Workload("d2", 4096, 7168, 128, "e4m3", "ue8m0", "row", False, 2,
+                   "normal, 0.1% x100 outliers", op="dequant"),
+    "b2": Workload("b2", 4096, 7168, 128, "e4m3", "ue8m0", "row", False, 2,
+                   "normal, 0.1% x100 outliers", op="cast_back"),
 }
 
 

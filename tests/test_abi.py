@@ -91,7 +91,61 @@ def test_validation(lib, name, kw, want):
     assert call(lib, **kw) == want
 
 
+def call_dq(lib, *, codes=A, ld_codes=256, scales=C, ld_scales=2, M=4, K=256,
+            group=128, fmt=0, mode=0, layout=0, y=B, ld_y=256, out=0):
+    return lib.tk_per_token_dequant(codes, ld_codes, scales, ld_scales, M, K,
+                                    group, fmt, mode, layout, y, ld_y, out,
+                                    None)
+
+
+DQ_CASES = [
+    ("bad out dtype", dict(out=2), INVALID),
+    ("bad group", dict(group=8), INVALID),
+    ("ld_codes < K", dict(ld_codes=128), INVALID),
+    ("ld_y < K", dict(ld_y=128), INVALID),
+    ("scales too narrow", dict(ld_scales=1), INVALID),
+    ("null y", dict(y=None), INVALID),
+    ("null codes", dict(codes=None), INVALID),
+    ("codes misaligned", dict(codes=A + 8), MISALIGNED),
+    ("y misaligned", dict(y=B + 4), MISALIGNED),
+    ("bf16 ld_y not 16 bytes", dict(K=128, ld_y=132, ld_scales=1), MISALIGNED),
+    ("fp32 ld_y not 16 bytes", dict(K=128, ld_y=130, ld_scales=1, out=1),
+     MISALIGNED),
+    ("transposed ld not multiple of 4", dict(layout=1, M=5, ld_scales=5),
+     MISALIGNED),
+    ("M too large", dict(M=(1 << 30) + 1), UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", DQ_CASES, ids=[c[0] for c in DQ_CASES])
+def test_dequant_validation(lib, name, kw, want):
+    assert call_dq(lib, **kw) == want
+
+
+def call_cb(lib, *, x=A, M=4, K=256, ld_x=256, group=128, fmt=0, mode=0,
+            y=B, ld_y=256):
+    return lib.tk_per_token_cast_back(x, M, K, ld_x, group, fmt, mode, y,
+                                      ld_y, None)
+
+
+CB_CASES = [
+    ("bad mode", dict(mode=5), INVALID),
+    ("K not multiple of group", dict(K=200), INVALID),
+    ("ld_y < K", dict(ld_y=128), INVALID),
+    ("null x", dict(x=None), INVALID),
+    ("y misaligned", dict(y=B + 2), MISALIGNED),
+    ("ld_y not 16 bytes", dict(K=128, ld_x=128, ld_y=132), MISALIGNED),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", CB_CASES, ids=[c[0] for c in CB_CASES])
+def test_cast_back_validation(lib, name, kw, want):
+    assert call_cb(lib, **kw) == want
+
+
 def test_empty_batch_is_a_noop(lib):
+    assert call_dq(lib, M=0, codes=None, scales=None, y=None) == OK
+    assert call_cb(lib, M=0, x=None, y=None) == OK
     assert call(lib, M=0, x=None, codes=None, scales=None) == OK
     assert call(lib, M=0, x=None, codes=None, scales=None, swiglu=True,
                 ld_x=512) == OK
