@@ -78,6 +78,12 @@ def _configure(lib):
     lib.oracle_per_token_cast_back.argtypes = [p, i64, i64, i64, i64, i, i, i,
                                                p, i64]
     lib.oracle_per_token_cast_back.restype = i
+    lib.oracle_per_block_cast.argtypes = [p, i64, i64, i64, i, i64, i64, i, i,
+                                          p, i64, p, i64]
+    lib.oracle_per_block_cast.restype = i
+    lib.oracle_per_channel_cast.argtypes = [p, i64, i64, i64, i64, i64, i, i,
+                                            p, i64, p]
+    lib.oracle_per_channel_cast.restype = i
     return lib
 
 
@@ -269,6 +275,96 @@ def per_token_cast_back(x_bits: np.ndarray, K: int, group: int, fmt: int,
 
     _split(M, threads, work)
     return y
+
+
+def block_scale_shape(M: int, K: int, block: int, mode: int):
+    """(rows, cols, dtype) of the per-block scale tensor: one row per block
+    row, one fp32 word per block column or ceil(blocks / 4) packed UE8M0
+    words."""
+    nr = (M + block - 1) // block
+    nc = (K + block - 1) // block
+    if mode == SCALE_UE8M0:
+        return nr, (nc + 3) // 4, np.int32
+    return nr, nc, np.float32
+
+
+def channel_scale_shape(K: int, mode: int):
+    """(length, dtype) of the per-channel scale vector."""
+    if mode == SCALE_UE8M0:
+        return (K + 3) // 4, np.int32
+    return K, np.float32
+
+
+def _codes_for(M, K, fmt, codes):
+    if codes is None:
+        codes = np.zeros((M, K if fmt == FMT_E4M3 else K // 2), np.uint8)
+    return codes
+
+
+def _check(rcs):
+    for rc in rcs:
+        if rc != 0:
+            raise ValueError(f"oracle returned status {rc}")
+
+
+def per_block_cast(x_bits: np.ndarray, K: int, block: int, fmt: int,
+                   mode: int, *, codes: np.ndarray | None = None,
+                   scales: np.ndarray | None = None, threads: int = 1):
+    """Oracle per-block cast (square blocks of ``block`` rows x channels) of
+    a BF16 matrix given as uint16 bit patterns [M, ld_x].  Returns (codes,
+    scales) with scales shaped by ``block_scale_shape``; block rows are
+    split across host threads."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits) if x_bits.strides[1] != 2 else x_bits
+    M = x_bits.shape[0]
+    ld_x = x_bits.strides[0] // 2
+    codes = _codes_for(M, K, fmt, codes)
+    if scales is None:
+        r, c, dt = block_scale_shape(M, K, block, mode)
+        scales = np.zeros((r, c), dt)
+    n_rb = (M + block - 1) // block
+    threads = max(1, min(threads or 1, n_rb))
+    bounds = np.linspace(0, n_rb, threads + 1).astype(np.int64)
+    ld_s = scales.strides[0] // 4
+
+    def work(t):
+        return lib.oracle_per_block_cast(
+            _ptr(x_bits), M, K, ld_x, block, int(bounds[t]),
+            int(bounds[t + 1]), fmt, mode, _ptr(codes), codes.strides[0],
+            _ptr(scales), ld_s)
+
+    _check([work(0)] if threads == 1 else
+           list(_executor(threads).map(work, range(threads))))
+    return codes, scales
+
+
+def per_channel_cast(x_bits: np.ndarray, K: int, fmt: int, mode: int, *,
+                     codes: np.ndarray | None = None,
+                     scales: np.ndarray | None = None, threads: int = 1):
+    """Oracle per-channel cast (one scale per channel over all rows) of a
+    BF16 matrix given as uint16 bit patterns [M, ld_x].  Returns (codes,
+    scale vector shaped by ``channel_scale_shape``); channels are split
+    across host threads in multiples of 8."""
+    lib = _load()
+    M = x_bits.shape[0]
+    ld_x = x_bits.strides[0] // 2
+    codes = _codes_for(M, K, fmt, codes)
+    if scales is None:
+        n, dt = channel_scale_shape(K, mode)
+        scales = np.zeros(n, dt)
+    n8 = (K + 7) // 8
+    threads = max(1, min(threads or 1, n8))
+    bounds = [min(K, 8 * b) for b in
+              np.linspace(0, n8, threads + 1).astype(np.int64)]
+
+    def work(t):
+        return lib.oracle_per_channel_cast(
+            _ptr(x_bits), M, K, ld_x, int(bounds[t]), int(bounds[t + 1]),
+            fmt, mode, _ptr(codes), codes.strides[0], _ptr(scales))
+
+    _check([work(0)] if threads == 1 else
+           list(_executor(threads).map(work, range(threads))))
+    return codes, scales
 
 
 def swiglu_value(gate: float, up: float) -> float:

@@ -497,6 +497,158 @@ int oracle_per_token_cast_back(const uint16_t *x, int64_t m_begin,
     return rc;
 }
 
+/* ------------------------------------------ per-block and per-channel cast */
+
+/*
+ * TileKernels README (pypi tile-kernels 2.0.0), section "Features", and the
+ * hysenlabs page "TileKernels, TileLang kernels for MoE routing and
+ * low-precision quantization", section "Seven kernel families, from MoE
+ * routing to Sinkhorn normalisation": besides the per-token cast the
+ * library casts per block and per channel.  The pages name these and nothing more; the
+ * steps are the per-token ones with a different set of elements sharing a
+ * scale:
+ *   per block   : a square block of `block` rows x `block` channels (the
+ *                 library uses 128 x 128; the last block row and block
+ *                 column may be partial);
+ *   per channel : one channel (column) over all M rows.
+ * The amax, floor, scale and code steps are compute_scale and the
+ * encoders above, unchanged.
+ */
+
+/* One code into a row of codes (E2M1: element 2i in the low nibble of byte
+ * i, element 2i+1 in the high nibble). */
+static void put_code(uint8_t *codes_row, int64_t col, int fmt, float q)
+{
+    if (fmt == OR_FMT_E4M3) {
+        codes_row[col] = e4m3_encode(q);
+        return;
+    }
+    uint8_t c = e2m1_encode(q);
+    uint8_t *byte = &codes_row[col / 2];
+    if (col % 2 == 0)
+        *byte = (uint8_t)((*byte & 0xF0u) | c);
+    else
+        *byte = (uint8_t)((*byte & 0x0Fu) | (c << 4));
+}
+
+/* Entry i of a vector of scales: fp32 word i, or, for packed UE8M0, byte
+ * i % 4 of word i / 4 (little-endian: byte i of the vector's bytes). */
+static void put_scale(void *vec, int64_t i, int mode, group_scale sc)
+{
+    if (mode == OR_SCALE_UE8M0)
+        ((uint8_t *)vec)[i] = (uint8_t)sc.ue8m0;
+    else
+        ((float *)vec)[i] = sc.s;
+}
+
+/* Unused bytes of the last, partly filled packed UE8M0 word are zero. */
+static void zero_word_tail(void *vec, int64_t n)
+{
+    for (int64_t i = n; i % 4 != 0; ++i)
+        ((uint8_t *)vec)[i] = 0;
+}
+
+static int check_tile_args(int64_t M, int64_t K, int fmt, int mode)
+{
+    if (M < 0 || K <= 0)
+        return OR_BAD_ARG;
+    if (fmt != OR_FMT_E4M3 && fmt != OR_FMT_E2M1)
+        return OR_BAD_ARG;
+    if (fmt == OR_FMT_E2M1 && K % 2 != 0)
+        return OR_BAD_ARG;
+    if (mode < OR_SCALE_FP32 || mode > OR_SCALE_UE8M0)
+        return OR_BAD_ARG;
+    return OR_OK;
+}
+
+/*
+ * Per-block cast of block rows [rb_begin, rb_end).
+ *   x      : BF16 bit patterns, row m at x + m*ld_x, K values.
+ *   codes  : row m at codes + m*ld_codes (bytes), as the per-token cast.
+ *   scales : 4-byte words, block row rb at scales + rb*ld_scales words;
+ *            block column j is fp32 word j, or byte j of the row's packed
+ *            UE8M0 words (unused bytes of the last word zero).
+ */
+int oracle_per_block_cast(const uint16_t *x, int64_t M, int64_t K,
+                          int64_t ld_x, int block, int64_t rb_begin,
+                          int64_t rb_end, int fmt, int mode, uint8_t *codes,
+                          int64_t ld_codes, void *scales, int64_t ld_scales)
+{
+    if (block != 16 && block != 32 && block != 64 && block != 128)
+        return OR_BAD_ARG;
+    int rc = check_tile_args(M, K, fmt, mode);
+    if (rc != OR_OK)
+        return rc;
+    int64_t n_cb = (K + block - 1) / block;
+    for (int64_t rb = rb_begin; rb < rb_end; ++rb) {
+        int64_t r0 = rb * block;
+        int64_t r1 = r0 + block < M ? r0 + block : M;
+        uint8_t *srow = (uint8_t *)scales + rb * ld_scales * 4;
+        for (int64_t cb = 0; cb < n_cb; ++cb) {
+            int64_t c0 = cb * block;
+            int64_t c1 = c0 + block < K ? c0 + block : K;
+            float bmax = 0.0f;
+            for (int64_t r = r0; r < r1; ++r) {
+                for (int64_t c = c0; c < c1; ++c) {
+                    float v = bf16_bits_to_float(x[r * ld_x + c]);
+                    if (!isfinite(v))
+                        return OR_NONFINITE;
+                    if (fabsf(v) > bmax)
+                        bmax = fabsf(v);
+                }
+            }
+            group_scale sc = compute_scale(bmax, fmt, mode);
+            for (int64_t r = r0; r < r1; ++r)
+                for (int64_t c = c0; c < c1; ++c)
+                    put_code(codes + r * ld_codes, c, fmt,
+                             bf16_bits_to_float(x[r * ld_x + c]) / sc.s);
+            put_scale(srow, cb, mode, sc);
+        }
+        if (mode == OR_SCALE_UE8M0)
+            zero_word_tail(srow, n_cb);
+    }
+    return OR_OK;
+}
+
+/*
+ * Per-channel cast of channels [k_begin, k_end) over all M rows.
+ *   scales : a vector, channel k at fp32 word k or byte k of the packed
+ *            UE8M0 words (the unused bytes of the last word are zeroed by
+ *            the call whose range ends at K).
+ * Callers splitting the channels keep k_begin a multiple of 4 (two E2M1
+ * codes share a byte; four UE8M0 bytes share a word).  M == 0 writes
+ * nothing: there is no element to take a scale from.
+ */
+int oracle_per_channel_cast(const uint16_t *x, int64_t M, int64_t K,
+                            int64_t ld_x, int64_t k_begin, int64_t k_end,
+                            int fmt, int mode, uint8_t *codes,
+                            int64_t ld_codes, void *scales)
+{
+    int rc = check_tile_args(M, K, fmt, mode);
+    if (rc != OR_OK)
+        return rc;
+    if (M == 0)
+        return OR_OK;
+    for (int64_t k = k_begin; k < k_end; ++k) {
+        float cmax = 0.0f;
+        for (int64_t m = 0; m < M; ++m) {
+            float v = bf16_bits_to_float(x[m * ld_x + k]);
+            if (!isfinite(v))
+                return OR_NONFINITE;
+            if (fabsf(v) > cmax)
+                cmax = fabsf(v);
+        }
+        group_scale sc = compute_scale(cmax, fmt, mode);
+        for (int64_t m = 0; m < M; ++m)
+            put_code(codes + m * ld_codes, k, fmt,
+                     bf16_bits_to_float(x[m * ld_x + k]) / sc.s);
+        put_scale(scales, k, mode, sc);
+    }
+    if (mode == OR_SCALE_UE8M0 && k_end == K)
+        zero_word_tail(scales, K);
+    return OR_OK;
+}
+
 /* ------------------------------------------- element-level hooks for pins */
 
 /* Saturating RNE encode of n fp32 values (the code step of the cast alone). */

@@ -16,6 +16,7 @@ import test_oracle_codec as tk
 import test_oracle_dequant as td
 import test_oracle_scale as ts
 import test_oracle_swiglu as tw
+import test_oracle_tile_cast as tt
 
 MUTATIONS = {
     "ties_away_e4m3": ("(dropped == 0x80000u && (keep & 1u))",
@@ -57,10 +58,31 @@ MUTATIONS = {
                                        "                                         : base[m * 0 + j * ld_scales];"),
 }
 
+# Mistakes in the per-block / per-channel code, run against those pins.
+TILE_MUTATIONS = {
+    "block_last_row_dropped": ("int64_t r1 = r0 + block < M ? r0 + block : M;",
+                               "int64_t r1 = r0 + block - 1 < M ? r0 + block - 1 : M;"),
+    "block_amax_last_column_missed": ("for (int64_t c = c0; c < c1; ++c) {\n                    float v",
+                                      "for (int64_t c = c0; c < c1 - 1; ++c) {\n                    float v"),
+    "block_scale_columns_reversed": ("put_scale(srow, cb, mode, sc);",
+                                     "put_scale(srow, n_cb - 1 - cb, mode, sc);"),
+    "block_pad_not_zeroed": ("            zero_word_tail(srow, n_cb);", "            (void)srow;"),
+    "block_rows_share_scale_row": ("uint8_t *srow = (uint8_t *)scales + rb * ld_scales * 4;",
+                                   "uint8_t *srow = (uint8_t *)scales + (rb / 2) * ld_scales * 4;"),
+    "channel_amax_last_row_missed": ("for (int64_t m = 0; m < M; ++m) {\n            float v",
+                                     "for (int64_t m = 0; m < M - 1; ++m) {\n            float v"),
+    "channel_amax_signed": ("if (fabsf(v) > cmax)\n                cmax = fabsf(v);",
+                            "if (v > cmax)\n                cmax = v;"),
+    "channel_pad_not_zeroed": ("        zero_word_tail(scales, K);", "        (void)scales;"),
+    "tile_nibble_order": ("if (col % 2 == 0)", "if (col % 2 == 1)"),
+    "tile_scale_multiplied": ("bf16_bits_to_float(x[m * ld_x + k]) / sc.s);",
+                              "bf16_bits_to_float(x[m * ld_x + k]) * sc.s);"),
+}
 
-def _pin_functions():
+
+def _pin_functions(mods=None):
     fns = []
-    for mod in (tk, ts, tc, tw, td):
+    for mod in mods or (tk, ts, tc, tw, td):
         for name, fn in inspect.getmembers(mod, inspect.isfunction):
             if name.startswith("test_") and fn.__module__ == mod.__name__:
                 fns.append(fn)
@@ -97,6 +119,27 @@ def test_planted_mistake_is_caught(name, tmp_path):
     failed = []
     try:
         for fn in _pin_functions():
+            try:
+                _call_all_params(fn)
+            except Exception:  # any failing pin counts
+                failed.append(fn.__name__)
+    finally:
+        oracle._lib = real
+    assert failed, f"no pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", sorted(TILE_MUTATIONS))
+def test_planted_tile_mistake_is_caught(name, tmp_path):
+    old, new = TILE_MUTATIONS[name]
+    src = oracle.source_text()
+    assert old in src, f"mutation anchor not found: {old!r}"
+    lib = oracle.compile_variant(src.replace(old, new, 1),
+                                 str(tmp_path / f"lib_{name}.so"))
+    real = oracle._load()
+    oracle._lib = lib
+    failed = []
+    try:
+        for fn in _pin_functions((tt,)):
             try:
                 _call_all_params(fn)
             except Exception:  # any failing pin counts
