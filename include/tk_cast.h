@@ -23,10 +23,11 @@
  *  - All data pointers are DEVICE pointers (global memory of the current
  *    CUDA device).  The caller allocates and owns every buffer; the library
  *    allocates nothing and keeps no pointer after the call returns.
- *  - Calls are asynchronous: they validate on the host, enqueue one kernel
+ *  - Calls are asynchronous: they validate on the host, enqueue their work
  *    on `stream` (a cudaStream_t passed as void*, NULL = legacy default
- *    stream) and return.  Outputs are ready once the stream reaches that
- *    point.  Input and outputs must not overlap.
+ *    stream; one kernel, except tk_per_channel_cast) and return.  Outputs
+ *    are ready once the stream reaches that point.  Input and outputs must
+ *    not overlap.
  *  - Inputs must be finite; NaN/Inf inputs give unspecified codes/scales.
  *  - Errors are returned, never raised: nothing aborts or throws across
  *    the ABI, and nothing is launched when a check fails.
@@ -43,6 +44,7 @@
 #ifndef TK_CAST_H
 #define TK_CAST_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 /* Exported from the shared library even when it is built with hidden
@@ -177,9 +179,68 @@ TK_API tk_status tk_per_token_cast_back(const void *x, int64_t M, int64_t K,
                                         int mode, void *y, int64_t ld_y,
                                         void *stream);
 
+/* Block edge of tk_per_block_cast (square blocks of rows x channels), and
+ * the channel granularity of tk_per_channel_cast's workspace. */
+#define TK_BLOCK 128
+
+/*
+ * tk_per_block_cast -- per-block cast (TileKernels README, "Features":
+ * "per-block ... FP8/FP4 casting"; the pages give no block shape, and this
+ * library uses square TK_BLOCK x TK_BLOCK blocks of rows x channels).
+ *
+ *   Block (i, j) is rows [128 i, 128 i + 128) x channels [128 j, 128 j + 128),
+ *   clipped to the matrix (the last block row and column may be partial).
+ *   Its elements share one scale, computed as in tk_per_token_cast from the
+ *   amax over the whole block; codes as tk_per_token_cast writes them.
+ *
+ *   x         BF16 [M][ld_x], K values used per row; K % 16 == 0, ld_x >= K.
+ *   codes     uint8 [M][ld_codes]: K bytes (E4M3) or K/2 bytes (E2M1) per row.
+ *   scales    4-byte words, [ceil(M/128)][ld_scales]: block (i, j) is fp32
+ *             word j of row i, or, for TK_SCALE_UE8M0_PACKED, byte j of row
+ *             i's packed words (byte j % 4 of word j / 4; the unused bytes of
+ *             a row's last word are set to 0).  ld_scales >= ceil(K/128)
+ *             (fp32 modes) or >= ceil(ceil(K/128) / 4) (packed).
+ *   fmt, mode tk_format, tk_scale_mode; scales are always row-major.
+ */
+TK_API tk_status tk_per_block_cast(const void *x, int64_t M, int64_t K,
+                                   int64_t ld_x, int fmt, int mode,
+                                   void *codes, int64_t ld_codes,
+                                   void *scales, int64_t ld_scales,
+                                   void *stream);
+
+/* Bytes of workspace tk_per_channel_cast needs for K channels: 12 per
+ * channel, K rounded up to a multiple of TK_BLOCK (0 if K is out of range). */
+TK_API size_t tk_per_channel_workspace_bytes(int64_t K);
+
+/*
+ * tk_per_channel_cast -- per-channel cast (TileKernels README, "Features":
+ * "per-channel ... FP8/FP4 casting"): channel k (column k) shares one scale
+ * over all M rows, computed as in tk_per_token_cast from the column's amax;
+ * codes as tk_per_token_cast writes them.
+ *
+ *   x, codes  as for tk_per_block_cast (K % 16 == 0).
+ *   scales    a vector: K fp32 words, or ceil(K/4) int32 words of packed
+ *             UE8M0 bytes (channel k in byte k % 4 of word k / 4).  4-byte
+ *             aligned.
+ *   workspace device memory of at least tk_per_channel_workspace_bytes(K)
+ *             bytes, 16-byte aligned, owned by the caller.  Its contents on
+ *             entry do not matter; the call overwrites them (column maxima,
+ *             scales and their reciprocals).  Calls that may run at the same
+ *             time (other streams) must not share a workspace.
+ *   Enqueues on `stream` a memset of the workspace's column maxima and
+ *   three kernels (column amax, column scales, cast); x is read twice.
+ *   M == 0 writes nothing (no element to take a scale from).
+ */
+TK_API tk_status tk_per_channel_cast(const void *x, int64_t M, int64_t K,
+                                     int64_t ld_x, int fmt, int mode,
+                                     void *codes, int64_t ld_codes,
+                                     void *scales, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
 /*
  * tk_get_device_fault -- read (and optionally clear) the library's device
- * fault word on the current device.  Every wait inside the kernels is
+ * fault words on the current device (the OR of the per-token kernels' word
+ * and the per-block / per-channel kernels' word).  Every wait inside the kernels is
  * bounded in time (1 s); a wait that runs out makes the kernel stop, let its
  * own in-flight copies land and return, OR-ing a code into this word:
  *   1 = a consumer waited too long for a tile, 2 = the producer waited too

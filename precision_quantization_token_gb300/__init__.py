@@ -14,6 +14,11 @@ Low level (same names and arguments as the C ABI, raw pointers and sizes):
                          group, fmt, mode, layout, y_ptr, ld_y, out_dtype, stream)
     tk_per_token_cast_back(x_ptr, M, K, ld_x, group, fmt, mode, y_ptr, ld_y,
                            stream)
+    tk_per_block_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
+                      scales_ptr, ld_scales, stream)
+    tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
+                        scales_ptr, workspace_ptr, workspace_bytes, stream)
+    tk_per_channel_workspace_bytes(K)
 
 Tensor level (allocates outputs with torch):
     codes, scales = per_token_cast(x, group=128, fmt="e4m3", scale="fp32",
@@ -21,6 +26,8 @@ Tensor level (allocates outputs with torch):
     codes, scales = swiglu_per_token_cast(x, group=128, ...)  # x = [gate|up]
     y = per_token_dequant(codes, scales, K, group=128, fmt="e4m3", ...)
     y = per_token_cast_back(x, group=128, fmt="e4m3", scale="fp32")
+    codes, scales = per_block_cast(x, fmt="e4m3", scale="fp32")   # 128x128
+    codes, scales = per_channel_cast(x, fmt="e4m3", scale="fp32")
 
 Operation (TileKernels README, "Features"; aiwiki "TileKernels", section
 "Quantization"): per row and per group of 16/32/64/128 channels, amax, a
@@ -90,6 +97,14 @@ def load():
             lib.tk_per_token_dequant.argtypes = [p, i64, p, i64, i64, i64, i, i,
                                                  i, i, p, i64, i, p]
             lib.tk_per_token_dequant.restype = i
+            lib.tk_per_block_cast.argtypes = [p, i64, i64, i64, i, i, p, i64,
+                                              p, i64, p]
+            lib.tk_per_block_cast.restype = i
+            lib.tk_per_channel_cast.argtypes = [p, i64, i64, i64, i, i, p, i64,
+                                                p, p, ctypes.c_size_t, p]
+            lib.tk_per_channel_cast.restype = i
+            lib.tk_per_channel_workspace_bytes.argtypes = [i64]
+            lib.tk_per_channel_workspace_bytes.restype = ctypes.c_size_t
             lib.tk_get_device_fault.argtypes = [p, i]
             lib.tk_get_device_fault.restype = i
             lib.tk_status_string.argtypes = [i]
@@ -143,6 +158,26 @@ def tk_per_token_dequant(codes_ptr, ld_codes, scales_ptr, ld_scales, M, K,
                                        layout, y_ptr, ld_y, out_dtype, stream))
 
 
+def tk_per_block_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
+                      scales_ptr, ld_scales, stream=0) -> None:
+    """Raw-pointer call of the per-block (128 x 128) cast."""
+    _check(load().tk_per_block_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr,
+                                    ld_codes, scales_ptr, ld_scales, stream))
+
+
+def tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
+                        scales_ptr, workspace_ptr, workspace_bytes,
+                        stream=0) -> None:
+    """Raw-pointer call of the per-channel cast (caller's workspace)."""
+    _check(load().tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr,
+                                      ld_codes, scales_ptr, workspace_ptr,
+                                      workspace_bytes, stream))
+
+
+def tk_per_channel_workspace_bytes(K: int) -> int:
+    return int(load().tk_per_channel_workspace_bytes(K))
+
+
 def tk_get_device_fault(clear: bool = False) -> int:
     """The device fault word of the current device (0: no kernel gave up on
     a wait); see include/tk_cast.h."""
@@ -169,10 +204,17 @@ def scale_shape(M: int, K: int, group: int, scale: str = "fp32",
     return (words, m_pad), dtype
 
 
-def _outputs(torch, M, K, group, fmt, scale, layout, device, codes, scales):
+def _code_buffer(torch, M, K, fmt, device):
+    """uint8 [M, K or K/2] codes whose rows start on 16-byte boundaries (a
+    view of a buffer with the row stride rounded up to 16 bytes)."""
     row_bytes = K if fmt == "e4m3" else K // 2
+    ld = (row_bytes + 15) // 16 * 16
+    return torch.empty((M, ld), dtype=torch.uint8, device=device)[:, :row_bytes]
+
+
+def _outputs(torch, M, K, group, fmt, scale, layout, device, codes, scales):
     if codes is None:
-        codes = torch.empty((M, row_bytes), dtype=torch.uint8, device=device)
+        codes = _code_buffer(torch, M, K, fmt, device)
     if scales is None:
         shape, dt = scale_shape(M, K, group, scale, layout)
         scales = torch.empty(shape, dtype=getattr(torch, dt), device=device)
@@ -272,3 +314,83 @@ def per_token_cast_back(x, group: int = 128, fmt: str = "e4m3",
     tk_per_token_cast_back(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt],
                            SCALE[scale], out.data_ptr(), out.stride(0), stream)
     return out
+
+
+BLOCK = 128   # edge of the per-block cast's square blocks (TK_BLOCK)
+
+
+def block_scale_shape(M: int, K: int, scale: str = "fp32"):
+    """Shape and torch dtype name of the per-block scale tensor."""
+    nr, nc = -(-M // BLOCK), -(-K // BLOCK)
+    if scale == "ue8m0":
+        return (nr, (nc + 3) // 4), "int32"
+    return (nr, nc), "float32"
+
+
+def channel_scale_shape(K: int, scale: str = "fp32"):
+    """Shape and torch dtype name of the per-channel scale vector."""
+    if scale == "ue8m0":
+        return ((K + 3) // 4,), "int32"
+    return (K,), "float32"
+
+
+def _check_x(x):
+    import torch
+    if (x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1
+            or x.device.type != "cuda"):
+        raise ValueError("x must be a 2-D bfloat16 CUDA tensor with unit "
+                         "column stride")
+
+
+def _codes(torch, x, fmt, codes):
+    if codes is None:
+        M, K = x.shape
+        codes = _code_buffer(torch, M, K, fmt, x.device)
+    return codes
+
+
+def per_block_cast(x, fmt: str = "e4m3", scale: str = "fp32", *, codes=None,
+                   scales=None, stream=None):
+    """Per-block cast of a bfloat16 [M, K] CUDA tensor: one scale per
+    128 x 128 block.  Returns (codes [M, K or K/2], scales, see
+    ``block_scale_shape``); asynchronous on the current stream."""
+    import torch
+    _check_x(x)
+    M, K = x.shape
+    codes = _codes(torch, x, fmt, codes)
+    if scales is None:
+        shape, dt = block_scale_shape(M, K, scale)
+        scales = torch.empty(shape, dtype=getattr(torch, dt), device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    tk_per_block_cast(x.data_ptr(), M, K, x.stride(0), FMT[fmt], SCALE[scale],
+                      codes.data_ptr(), codes.stride(0), scales.data_ptr(),
+                      scales.stride(0), stream)
+    return codes, scales
+
+
+def per_channel_cast(x, fmt: str = "e4m3", scale: str = "fp32", *,
+                     codes=None, scales=None, workspace=None, stream=None):
+    """Per-channel cast of a bfloat16 [M, K] CUDA tensor: one scale per
+    column over all rows.  Returns (codes, scale vector, see
+    ``channel_scale_shape``).  ``workspace`` (uint8 CUDA tensor of at least
+    ``tk_per_channel_workspace_bytes(K)`` bytes) is allocated per call when
+    not given; calls in flight together must not share one."""
+    import torch
+    _check_x(x)
+    M, K = x.shape
+    codes = _codes(torch, x, fmt, codes)
+    if scales is None:
+        shape, dt = channel_scale_shape(K, scale)
+        scales = torch.empty(shape, dtype=getattr(torch, dt), device=x.device)
+    need = tk_per_channel_workspace_bytes(K)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
+                                device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    tk_per_channel_cast(x.data_ptr(), M, K, x.stride(0), FMT[fmt],
+                        SCALE[scale], codes.data_ptr(), codes.stride(0),
+                        scales.data_ptr(), workspace.data_ptr(),
+                        workspace.numel(), stream)
+    return codes, scales

@@ -1,8 +1,9 @@
 """Compile the CUDA library (csrc/*.cu) into an in-tree shared object.
 
-One nvcc invocation, one -gencode (sm_103a), no fast-math.  The result lives
-at precision_quantization_token_gb300/_build/libtk_cast.so and is loaded by
-the ctypes binding in __init__.py.
+Each translation unit is compiled by its own nvcc process (in parallel) with
+one -gencode (sm_103a) and no fast-math, then nvcc links the objects.  The
+result lives at precision_quantization_token_gb300/_build/libtk_cast.so and
+is loaded by the ctypes binding in __init__.py.
 """
 from __future__ import annotations
 
@@ -18,13 +19,14 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libtk_cast.so")
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
-NVCC_FLAGS = [
+COMPILE_FLAGS = [
     ARCH, "-O3", "-lineinfo", "-std=c++17",
     "-ftz=false", "-prec-div=true", "-prec-sqrt=true", "-fmad=false",
     "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-    "-Xcompiler", "-Wall", "-Xcompiler", "-Wextra",
-    "-shared", f"-I{INCLUDE}",
+    "-Xcompiler", "-Wall", "-Xcompiler", "-Wextra", f"-I{INCLUDE}",
 ]
+# One-shot form (compile and link every source in one nvcc call).
+NVCC_FLAGS = COMPILE_FLAGS + ["-shared"]
 
 
 def sources() -> list[str]:
@@ -56,12 +58,26 @@ def build(force: bool = False, verbose: bool = False,
     if not force and not extra and up_to_date():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = [nvcc(), *NVCC_FLAGS, *(extra or []), "-o", tmp, *sources()]
-    if verbose:
-        print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    tag = f"{os.getpid()}.tmp"
+    objs, procs = [], []
+    for src in sources():
+        obj = os.path.join(BUILD_DIR, os.path.basename(src) + f".{tag}.o")
+        cmd = [nvcc(), *COMPILE_FLAGS, *(extra or []), "-c", "-o", obj, src]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        objs.append(obj)
+        procs.append((cmd, subprocess.Popen(cmd)))
+    failed = [cmd for cmd, p in procs if p.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = LIB_PATH + f".{tag}"
+        subprocess.run([nvcc(), ARCH, "-shared", "-o", tmp, *objs], check=True)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB_PATH
 
 

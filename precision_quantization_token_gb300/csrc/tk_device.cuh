@@ -1,0 +1,299 @@
+// Device building blocks shared by the cast kernels (sm_103a): mbarrier
+// and bulk-copy primitives with bounded waits, BF16 widening, the hardware
+// E4M3 / E2M1 conversions and decodes, and the IEEE fp32 scale and quotient
+// steps.  Internal to the library; every file that includes it gets its own
+// copies (everything here is in an anonymous namespace).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tk_cast.h"
+
+namespace {
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s per wait
+
+// Fault codes recorded by a kernel whose wait ran out (OR-ed together).
+constexpr unsigned kFaultConsumerWait = 1u;
+constexpr unsigned kFaultProducerWait = 2u;
+constexpr unsigned kFaultDrain = 4u;
+
+// -------------------------------------------------------- PTX primitives
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}"
+               ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+      ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete, for at most
+// kWaitLimitNs, giving up early if another warp has raised `abort_flag`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (abort_flag != nullptr && *abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// Bulk prefetch of global bytes into L2.  A hint: it reads nothing into the
+// program's state and orders nothing, so it may run before a dependency wait.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Bulk asynchronous copy global -> shared (this CTA), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
+                                          uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds8(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Two BF16 values in one 32-bit word -> two fp32 values (exact widening).
+__device__ __forceinline__ void widen2(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xFFFF0000u);
+}
+
+// BF16 element e (a compile-time index after unrolling) of a loaded chunk.
+template <int N8>
+__device__ __forceinline__ float bf16_at(const uint4 (&r)[N8], int e) {
+  const uint4 q = r[e / 8];
+  const int w = (e % 8) / 2;
+  const uint32_t word = w == 0 ? q.x : w == 1 ? q.y : w == 2 ? q.z : q.w;
+  return __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
+}
+
+template <int N8>
+__device__ __forceinline__ void widen(const uint4 (&raw)[N8], float (&v)[N8 * 8]) {
+#pragma unroll
+  for (int i = 0; i < N8; ++i) {
+    widen2(raw[i].x, v[8 * i + 0], v[8 * i + 1]);
+    widen2(raw[i].y, v[8 * i + 2], v[8 * i + 3]);
+    widen2(raw[i].z, v[8 * i + 4], v[8 * i + 5]);
+    widen2(raw[i].w, v[8 * i + 6], v[8 * i + 7]);
+  }
+}
+
+// ------------------------------------------------------------ conversions
+
+// Four fp32 -> four E4M3 bytes, element 0 in the lowest byte.  In the cvt,
+// the first source lands in the upper half of the 16-bit result.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c,
+                                               float d) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(out)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return out;
+}
+
+// Eight fp32 -> eight E2M1 nibbles in one word, element 0 in bits 3:0.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float* v) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]),
+        "f"(v[6]), "f"(v[7]));
+  return out;
+}
+
+// Exact decode of codes to fp32 through the hardware f16x2 conversions
+// (every E4M3 and E2M1 value is an fp16 value): two E4M3 codes in the low
+// 16 bits of `two` (element 0 in the low byte); two E2M1 codes in the low 8
+// bits (element 0 in the low nibble).
+__device__ __forceinline__ float2 decode_e4m3x2(uint32_t two) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(h) : "r"(two));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ float2 decode_e2m1x2(uint32_t two) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 c;\n\tcvt.u8.u32 c, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, c;\n\t}" : "=r"(h) : "r"(two));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Sixteen E4M3 codes (one uint4) or E2M1 codes (one uint2) -> fp32 values.
+__device__ __forceinline__ void decode16_e4m3(const uint4& c, float (&v)[16]) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 lo = decode_e4m3x2(w[i] & 0xFFFFu);
+    const float2 hi = decode_e4m3x2(w[i] >> 16);
+    v[4 * i + 0] = lo.x;
+    v[4 * i + 1] = lo.y;
+    v[4 * i + 2] = hi.x;
+    v[4 * i + 3] = hi.y;
+  }
+}
+
+__device__ __forceinline__ void decode16_e2m1(const uint2& c, float (&v)[16]) {
+  const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 d = decode_e2m1x2((w[i] >> (8 * b)) & 0xFFu);
+      v[8 * i + 2 * b] = d.x;
+      v[8 * i + 2 * b + 1] = d.y;
+    }
+}
+
+// Two fp32 -> two BF16 (round to nearest even), element a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  uint32_t out;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out) : "f"(b), "f"(a));
+  return out;
+}
+
+// Sixteen values times s (one IEEE fp32 multiply each), stored at dst as
+// BF16 (32 bytes) or fp32 (64 bytes).
+__device__ __forceinline__ void store_scaled16(uint8_t* dst, const float (&v)[16],
+                                               float s, bool as_fp32) {
+  float y[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) y[k] = __fmul_rn(v[k], s);
+  if (as_fp32) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      d[i] = make_uint4(__float_as_uint(y[4 * i]), __float_as_uint(y[4 * i + 1]),
+                        __float_as_uint(y[4 * i + 2]), __float_as_uint(y[4 * i + 3]));
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      d[i] = make_uint4(pack_bf16x2(y[8 * i], y[8 * i + 1]), pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
+                        pack_bf16x2(y[8 * i + 4], y[8 * i + 5]), pack_bf16x2(y[8 * i + 6], y[8 * i + 7]));
+  }
+}
+
+// ------------------------------------------------------------ scale math
+
+struct GroupScale {
+  float s;        // the divisor
+  float inv;      // 2^-k (power-of-two modes) or RN(1/s) (fp32 mode)
+  uint32_t e;     // biased exponent 127 + k (power-of-two modes)
+};
+
+template <int FMT, bool POW2>
+__device__ __forceinline__ GroupScale group_scale(float amax) {
+  constexpr float kMax = FMT == TK_FMT_E4M3 ? 448.0f : 6.0f;
+  const float r = __fdiv_rn(fmaxf(amax, 1e-4f), kMax);
+  GroupScale g;
+  if constexpr (POW2) {
+    // r is a positive normal number (>= 1e-4/448); 2^ceil(log2 r) keeps its
+    // exponent when the mantissa is zero and bumps it otherwise.
+    const uint32_t u = __float_as_uint(r);
+    g.e = (u >> 23) + ((u & 0x7FFFFFu) != 0u);
+    g.s = __uint_as_float(g.e << 23);
+    g.inv = __uint_as_float((254u - g.e) << 23);   // e <= 253, so 2^-k is normal
+  } else {
+    g.s = r;
+    g.inv = __frcp_rn(r);
+    g.e = 0;
+  }
+  return g;
+}
+
+// True when every amax within a relative 2^-16 of m gives the same
+// power-of-two scale.  The scale is 2^ceil(log2(max(a, 1e-4) / fmt_max)),
+// which only changes where that ratio crosses a power of two; with
+// r ~ max(m, 1e-4) / fmt_max (one multiply, relative error below 2^-23), a
+// mantissa field at least 2^10 away from both ends of the binade keeps r
+// more than 2^-13 (relative) from every power of two, so no perturbation
+// of 2^-16 (nor the rounding of the division) can cross one.
+template <int FMT>
+__device__ __forceinline__ bool pow2_settled(float m) {
+  constexpr float kInvMax = FMT == TK_FMT_E4M3 ? 1.0f / 448.0f : 1.0f / 6.0f;
+  const uint32_t mant = __float_as_uint(fmaxf(m, 1e-4f) * kInvMax) & 0x7FFFFFu;
+  return mant > (1u << 10) && mant < (1u << 23) - (1u << 10);
+}
+
+// x / s rounded to nearest: exact product for a power-of-two scale, else the
+// reciprocal estimate q0 plus one residual correction q0 - (q0*s - x) * inv.
+// The residual is formed as q0*s - x and subtracted (rather than x - q0*s
+// added) so that x = -0 gives -0: every zero term then carries x's sign.  The
+// sequence is written in PTX so that no compiler rewrite (such as folding
+// the negation into the first FMA, which breaks signed zeros) can alter it.
+template <bool POW2>
+__device__ __forceinline__ float quotient(float x, const GroupScale& g) {
+  if constexpr (POW2) return x * g.inv;
+  float q;
+  asm("{\n\t.reg .f32 q0, r, nx;\n\t"
+      "mul.rn.f32 q0, %1, %2;\n\t"
+      "neg.f32 nx, %1;\n\t"
+      "fma.rn.f32 r, q0, %3, nx;\n\t"
+      "neg.f32 r, r;\n\t"
+      "fma.rn.f32 %0, r, %2, q0;\n\t}"
+      : "=f"(q)
+      : "f"(x), "f"(g.inv), "f"(g.s));
+  return q;
+}
+
+}  // namespace

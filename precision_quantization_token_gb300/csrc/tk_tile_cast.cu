@@ -1,0 +1,585 @@
+// GB300 (sm_103a) per-block and per-channel cast: BF16 -> FP8 E4M3 / FP4
+// E2M1 codes with one scale per 128 x 128 block, or one scale per channel
+// (column) over all rows.
+//
+// TileKernels lists per-block and per-channel FP8/FP4 casting beside the
+// per-token cast (README "Features"; hysenlabs page "TileKernels, TileLang
+// kernels for MoE routing and low-precision quantization", section "Seven
+// kernel families, from MoE routing to Sinkhorn normalisation").  The pages
+// give no block shape; this library uses square 128 x 128 blocks.  The
+// scale and code steps are the per-token cast's (tk_device.cuh): amax
+// floored at 1e-4, r = amax / fmt_max in IEEE fp32 (optionally rounded up
+// to a power of two, optionally stored as a UE8M0 byte), codes =
+// RNE(sat(x / s)).  include/tk_cast.h states the contract.
+//
+// Design (memory-bound, no tensor cores):
+//  * Tiles of 128 rows x 128 channels of BF16 (32 KiB) move into a ring of
+//    shared-memory stages with 2-D TMA tensor copies
+//    (cp.async.bulk.tensor.2d ... mbarrier::complete_tx) issued by one
+//    producer thread per CTA.  Rows past M and channels past K arrive as
+//    zeros (the tensor map's out-of-bounds fill), which changes no amax.
+//  * One persistent CTA per SM (the ring takes most of shared memory):
+//    6 stages and 3 consumer groups of 8 warps; group k takes this CTA's
+//    tiles k, k+3, ...  A warp owns 16 rows of a tile, a lane 8 channels of
+//    one of the two rows a warp step covers (16-byte shared loads; the 32
+//    lanes read 512 contiguous bytes, free of bank conflicts).
+//  * Per-block cast: a tile is one block.  Each warp loads its 8 x 16 bytes
+//    into registers and releases the stage at once, reduces its amax by
+//    shuffles, and the group combines its 8 warp maxima in shared memory
+//    behind a named barrier; every warp then casts from registers.
+//  * Per-channel cast: after the caller's workspace of column maxima is
+//    cleared, three launches:
+//      1. column amax: per tile, each group reduces the 128 column maxima of
+//         its 128 rows in shared memory and folds them into the workspace
+//         with atomicMax on the fp32 bit patterns (non-negative floats order
+//         like their bit patterns; max is exact and order-independent, so
+//         the result does not depend on timing);
+//      2. column scales: one thread per channel computes s and its
+//         reciprocal into the workspace and writes the caller's scale vector;
+//      3. cast: the tile pipeline again, each lane dividing its 8 channels
+//         by their own scales.
+//    Launches 1-3 are programmatic dependents: each waits
+//    (griddepcontrol.wait) for its predecessor before touching memory.
+//  * Every wait is bounded in time; on expiry the kernel records a fault
+//    code (tk_get_device_fault), stops, lets its own copies land and
+//    returns.  The groups agree on stopping through a barrier reduction, so
+//    no warp is left waiting at a named barrier.
+
+#include <cuda.h>            // CUtensorMap and its enums (types only)
+#include <cudaTypedefs.h>    // PFN_cuTensorMapEncodeTiled
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "tk_cast.h"
+#include "tk_device.cuh"
+#include "tk_internal.h"
+
+namespace {
+
+using tk_internal::aligned;
+using tk_internal::cuda_fail;
+
+constexpr int kTileCols = TK_BLOCK;                 // channels per tile (256 B rows)
+constexpr int kTileRows = TK_BLOCK;                 // rows per tile (the block height)
+constexpr int kRowBytes = kTileCols * 2;
+constexpr int kTileBytes = kTileRows * kRowBytes;  // 32 KiB
+constexpr int kGroupWarps = 8;
+constexpr int kGroups = 3;
+constexpr int kStages = 6;
+constexpr int kConsumerWarps = kGroups * kGroupWarps;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kPrefetchTiles = 2;
+constexpr int kWarpRows = kTileRows / kGroupWarps;    // 16
+constexpr int kSteps = kWarpRows / 2;                 // 2 rows per warp step
+static_assert(kStages % kGroups == 0, "each stage belongs to one group");
+static_assert(kTileCols == 16 * 8, "16 lanes x 8 channels cover a tile row");
+
+// Shared memory, from a 1024-byte aligned base: the ring, the full and empty
+// mbarriers, an abort flag, and per group two buffers of 8 x 128 floats for
+// the cross-warp reductions.
+constexpr int kBarOffset = kStages * kTileBytes;
+constexpr int kFlagOffset = kBarOffset + 16 * kStages;
+constexpr int kRedOffset = kFlagOffset + 16;
+constexpr int kRedFloats = 2 * kGroupWarps * kTileCols;   // per group
+constexpr int kSmemBytes = kRedOffset + kGroups * kRedFloats * 4 + 1024;
+static_assert(kSmemBytes <= 232448, "fits the 227 KiB opt-in");
+
+// The kernels this file builds (one template instance each).
+constexpr int kBlockCast = 0;     // 128 x 128 blocks -> codes + block scales
+constexpr int kColumnAmax = 1;    // column maxima into the workspace
+constexpr int kChannelCast = 2;   // codes with per-column scales
+
+__device__ unsigned int g_tile_fault;   // read and cleared via tk_get_device_fault
+
+struct TileParams {
+  uint8_t* codes;            // row m at codes + m * ld_codes
+  int64_t ld_codes;
+  uint8_t* scales;           // block: 4-byte words, block row rb at rb * ld_scales
+  int64_t ld_scales;         //   words; channel: a vector of K entries
+  unsigned int* col_amax;    // channel: [k_pad] fp32 bit patterns
+  float* col_s;              // channel: [k_pad] scales then [k_pad] reciprocals
+  int M, K;
+  int n_cb;                  // tile (block) columns: ceil(K / 128)
+  int n_tiles;
+  int k_pad;                 // n_cb * 128
+  int ue8m0;                 // 1: packed exponent bytes, 0: fp32 words
+};
+
+// ------------------------------------------------------------ primitives
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map,
+                                            int c, int r, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(bar)
+      : "memory");
+}
+
+// L2 prefetch of one tile.  A hint: it changes no memory and orders nothing.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c, int r) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r) : "memory");
+}
+
+// Barrier `id` over one consumer group (its 8 warps), returning whether
+// any of them passed `pred`.  Also orders the group's shared-memory writes
+// before it with the reads after it.
+__device__ __forceinline__ bool group_any(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(kGroupWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float bf16_lane(const uint4& q, int e) {
+  const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
+  return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// Eight channels (one 16-byte chunk of a tile row) -> codes at dst: 8 bytes
+// (E4M3) or 4 bytes (E2M1, element 0 in the low nibble), channel e divided
+// by (s[e], inv[e]).
+template <int FMT, bool POW2>
+__device__ __forceinline__ void cast8(uint8_t* dst, const uint4& raw,
+                                      const float (&s)[8], const float (&inv)[8]) {
+  float q[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    GroupScale g;
+    g.s = s[e];
+    g.inv = inv[e];
+    g.e = 0;
+    q[e] = quotient<POW2>(bf16_lane(raw, e), g);
+  }
+  if constexpr (FMT == TK_FMT_E4M3) {
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(cvt_e4m3x4(q[0], q[1], q[2], q[3]), cvt_e4m3x4(q[4], q[5], q[6], q[7]));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = cvt_e2m1x8(q);
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ uint8_t* code_ptr(const TileParams& p, int row, int col) {
+  return p.codes + (int64_t)row * p.ld_codes + (FMT == TK_FMT_E4M3 ? col : col / 2);
+}
+
+// ------------------------------------------------------------ producer
+
+__device__ void tile_produce(const CUtensorMap* map, const TileParams& p,
+                             uint32_t ring, uint32_t full0, uint32_t empty0,
+                             volatile int* abort_flag, int my_tiles) {
+  // This grid may have been launched before the previous kernel in the
+  // stream finished (programmatic dependent launch).  The L2 prefetch of the
+  // first tiles is a hint and may run before the wait (L2 is where the
+  // previous kernel's writes land); every copy and, through the copies,
+  // every consumer access follows the wait.
+  const int n_prefetch = my_tiles < kPrefetchTiles ? my_tiles : kPrefetchTiles;
+  for (int i = 0; i < n_prefetch; ++i) {
+    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+    const int rb = t / p.n_cb;
+    tma_prefetch_2d(map, (t - rb * p.n_cb) * kTileCols, rb * kTileRows);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int issued = 0;
+  for (int i = 0; i < my_tiles; ++i) {
+    const int s = i % kStages;
+    const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+    if (i >= kStages && !mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag)) {
+      if (!*abort_flag) atomicOr(&g_tile_fault, kFaultProducerWait);
+      *abort_flag = 1;
+      break;
+    }
+    if (*abort_flag) break;
+    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+    const int rb = t / p.n_cb;
+    const uint32_t full = full0 + 8 * s;
+    mbar_arrive_expect_tx(full, kTileBytes);   // the whole box, zero fill included
+    tma_load_2d(ring + (uint32_t)(s * kTileBytes), map, (t - rb * p.n_cb) * kTileCols,
+                rb * kTileRows, full);
+    issued = i + 1;
+  }
+  // Let every copy this thread issued land before the CTA can exit.
+  for (int i = issued - 1; i >= 0 && i >= issued - kStages; --i) {
+    const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+    if (!mbar_wait(full0 + 8 * (i % kStages), ph, nullptr)) {
+      atomicOr(&g_tile_fault, kFaultDrain);
+      break;
+    }
+  }
+}
+
+// ------------------------------------------------------------ the kernel
+
+template <int FMT, bool POW2, int OP>
+__global__ void __launch_bounds__(kThreads, 1)
+tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+  const uint32_t full0 = base + kBarOffset;
+  const uint32_t empty0 = full0 + 8 * kStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kFlagOffset);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kGroupWarps);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  const int my_tiles = (p.n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) tile_produce(&map, p, base, full0, empty0, abort_flag, my_tiles);
+    return;
+  }
+
+  const int group = warp / kGroupWarps;
+  const int gw = warp % kGroupWarps;
+  const int half = lane >> 4;          // which of a step's two rows
+  const int chunk = lane & 15;         // 8-channel chunk of the tile row
+  float* red = reinterpret_cast<float*>(smem + kRedOffset) + group * kRedFloats;
+
+  for (int i = group, n = 0; i < my_tiles; i += kGroups, ++n) {
+    const int s = i % kStages;
+    const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+    bool ok = mbar_wait(full0 + 8 * s, ph, abort_flag);
+    if (!ok) {
+      if (!*abort_flag) atomicOr(&g_tile_fault, kFaultConsumerWait);
+      *abort_flag = 1;
+    }
+    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+    const int rb = t / p.n_cb;
+    const int cb = t - rb * p.n_cb;
+    const int r0 = rb * kTileRows + gw * kWarpRows + half;   // this lane's first row
+    const int col = cb * kTileCols + chunk * 8;               // this lane's first channel
+
+    uint4 v[kSteps];
+    if (ok) {
+      const uint32_t src = base + (uint32_t)(s * kTileBytes) +
+                           (uint32_t)((gw * kWarpRows + half) * kRowBytes + chunk * 16);
+#pragma unroll
+      for (int j = 0; j < kSteps; ++j) v[j] = lds16(src + (uint32_t)(2 * j * kRowBytes));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);   // data now in registers
+    }
+    float* buf = red + (n & 1) * (kGroupWarps * kTileCols);
+
+    if constexpr (OP == kBlockCast) {
+      float m = 0.0f;
+      if (ok) {
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(bf16_lane(v[j], e)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) buf[gw] = m;
+      }
+      if (group_any(1 + group, !ok)) break;
+      float bmax = buf[0];
+#pragma unroll
+      for (int w = 1; w < kGroupWarps; ++w) bmax = fmaxf(bmax, buf[w]);
+      const GroupScale g = group_scale<FMT, POW2>(bmax);
+      float sv[8], iv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sv[e] = g.s;
+        iv[e] = g.inv;
+      }
+      if (col < p.K) {
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j) {
+          const int row = r0 + 2 * j;
+          if (row < p.M) cast8<FMT, POW2>(code_ptr<FMT>(p, row, col), v[j], sv, iv);
+        }
+      }
+      if (gw == 0 && lane == 0) {
+        if (p.ue8m0) {
+          uint8_t* srow = p.scales + (int64_t)rb * p.ld_scales * 4;
+          srow[cb] = (uint8_t)g.e;
+          if (cb == p.n_cb - 1)   // unused bytes of the last packed word
+            for (int b = cb + 1; (b & 3) != 0; ++b) srow[b] = 0;
+        } else {
+          reinterpret_cast<float*>(p.scales)[(int64_t)rb * p.ld_scales + cb] = g.s;
+        }
+      }
+    } else if constexpr (OP == kColumnAmax) {
+      if (ok) {
+        float cm[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm[e] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) cm[e] = fmaxf(cm[e], fabsf(bf16_lane(v[j], e)));
+#pragma unroll
+        for (int e = 0; e < 8; ++e) cm[e] = fmaxf(cm[e], __shfl_xor_sync(0xFFFFFFFFu, cm[e], 16));
+        if (half == 0) {
+          float4* d = reinterpret_cast<float4*>(buf + gw * kTileCols + chunk * 8);
+          d[0] = make_float4(cm[0], cm[1], cm[2], cm[3]);
+          d[1] = make_float4(cm[4], cm[5], cm[6], cm[7]);
+        }
+      }
+      if (group_any(1 + group, !ok)) break;
+      const int c = gw * 32 + lane;          // one thread per tile column
+      if (c < kTileCols) {
+        float m = buf[c];
+#pragma unroll
+        for (int w = 1; w < kGroupWarps; ++w) m = fmaxf(m, buf[w * kTileCols + c]);
+        const int k = cb * kTileCols + c;
+        if (k < p.K && m > 0.0f) atomicMax(&p.col_amax[k], __float_as_uint(m));
+      }
+    } else {   // kChannelCast
+      if (!ok) break;
+      if (col < p.K) {
+        float sv[8], iv[8];
+        const float4* sp = reinterpret_cast<const float4*>(p.col_s + col);
+        const float4* ip = reinterpret_cast<const float4*>(p.col_s + p.k_pad + col);
+        const float4 s0 = sp[0], s1 = sp[1], i0 = ip[0], i1 = ip[1];
+        sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
+        sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
+        iv[0] = i0.x; iv[1] = i0.y; iv[2] = i0.z; iv[3] = i0.w;
+        iv[4] = i1.x; iv[5] = i1.y; iv[6] = i1.z; iv[7] = i1.w;
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j) {
+          const int row = r0 + 2 * j;
+          if (row < p.M) cast8<FMT, POW2>(code_ptr<FMT>(p, row, col), v[j], sv, iv);
+        }
+      }
+    }
+  }
+}
+
+// Per-channel step 2: the scale of each channel from its column amax.
+template <int FMT, bool POW2>
+__global__ void __launch_bounds__(256) column_scale_kernel(const TileParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int c = (int)blockIdx.x * 256 + (int)threadIdx.x;
+  if (c < p.K) {
+    const GroupScale g = group_scale<FMT, POW2>(__uint_as_float(p.col_amax[c]));
+    p.col_s[c] = g.s;
+    p.col_s[p.k_pad + c] = g.inv;
+    if (p.ue8m0)
+      p.scales[c] = (uint8_t)g.e;
+    else
+      reinterpret_cast<float*>(p.scales)[c] = g.s;
+  } else if (p.ue8m0 && c < ((p.K + 3) & ~3)) {
+    p.scales[c] = 0;   // unused bytes of the last packed word
+  }
+}
+
+// ------------------------------------------------------------ host side
+
+using TileKernel = void (*)(CUtensorMap, TileParams);
+using ScaleKernel = void (*)(TileParams);
+
+template <int OP>
+TileKernel pick_tile(int fmt, bool pow2) {
+  if (fmt == TK_FMT_E4M3)
+    return pow2 ? tile_cast_kernel<TK_FMT_E4M3, true, OP> : tile_cast_kernel<TK_FMT_E4M3, false, OP>;
+  return pow2 ? tile_cast_kernel<TK_FMT_E2M1, true, OP> : tile_cast_kernel<TK_FMT_E2M1, false, OP>;
+}
+
+ScaleKernel pick_scale(int fmt, bool pow2) {
+  if (fmt == TK_FMT_E4M3)
+    return pow2 ? column_scale_kernel<TK_FMT_E4M3, true> : column_scale_kernel<TK_FMT_E4M3, false>;
+  return pow2 ? column_scale_kernel<TK_FMT_E2M1, true> : column_scale_kernel<TK_FMT_E2M1, false>;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// Tensor map of a BF16 matrix [M rows][ld_x] with K valid channels, in
+// 128 x 128 boxes, zero fill outside the matrix.
+tk_status make_map(CUtensorMap* map, const void* x, int64_t M, int64_t K, int64_t ld_x) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr) return tk_internal::fail_message("cuTensorMapEncodeTiled is not available");
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)(ld_x * 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileCols, (cuuint32_t)kTileRows};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x),
+                              dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return tk_internal::fail_message("cuTensorMapEncodeTiled rejected the input matrix");
+  return TK_OK;
+}
+
+cudaLaunchConfig_t dependent_launch(cudaLaunchAttribute* attr, unsigned grid, unsigned threads,
+                                    size_t smem, void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+tk_status launch_tile(TileKernel fn, const CUtensorMap& map, const TileParams& p, void* stream) {
+  int sms = 0;
+  cudaError_t err = tk_internal::prepare_kernel(reinterpret_cast<const void*>(fn), kSmemBytes, &sms);
+  if (err != cudaSuccess) return cuda_fail(err);
+  const int grid = p.n_tiles < sms ? p.n_tiles : sms;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = dependent_launch(attr, (unsigned)grid, kThreads, kSmemBytes, stream);
+  err = cudaLaunchKernelEx(&cfg, fn, map, p);
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? TK_OK : cuda_fail(err);
+}
+
+// Checks shared by both entry points.
+tk_status check_tile_args(int64_t M, int64_t K, int64_t ld_x, int fmt, int mode,
+                          int64_t ld_codes) {
+  if (fmt != TK_FMT_E4M3 && fmt != TK_FMT_E2M1) return TK_ERR_INVALID_ARG;
+  if (mode < TK_SCALE_FP32 || mode > TK_SCALE_UE8M0_PACKED) return TK_ERR_INVALID_ARG;
+  if (M < 0 || K <= 0 || K % 16 != 0) return TK_ERR_INVALID_ARG;
+  if (M > (int64_t(1) << 30) || K > (int64_t(1) << 28)) return TK_ERR_UNSUPPORTED;
+  const int64_t code_bytes = fmt == TK_FMT_E4M3 ? K : K / 2;
+  if (ld_x < K || ld_codes < code_bytes) return TK_ERR_INVALID_ARG;
+  return TK_OK;
+}
+
+tk_status check_tile_pointers(const void* x, int64_t ld_x, const void* codes, int64_t ld_codes,
+                              const void* scales) {
+  if (x == nullptr || codes == nullptr || scales == nullptr) return TK_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ld_x * 2) % 16 != 0 || !aligned(codes, 16) || ld_codes % 16 != 0 ||
+      !aligned(scales, 4))
+    return TK_ERR_MISALIGNED;
+  return TK_OK;
+}
+
+TileParams base_params(int64_t M, int64_t K, int mode, void* codes, int64_t ld_codes,
+                       void* scales) {
+  TileParams p = {};
+  p.codes = static_cast<uint8_t*>(codes);
+  p.ld_codes = ld_codes;
+  p.scales = static_cast<uint8_t*>(scales);
+  p.M = (int)M;
+  p.K = (int)K;
+  p.n_cb = (int)((K + kTileCols - 1) / kTileCols);
+  p.k_pad = p.n_cb * kTileCols;
+  p.ue8m0 = mode == TK_SCALE_UE8M0_PACKED ? 1 : 0;
+  return p;
+}
+
+}  // namespace
+
+namespace tk_internal {
+
+tk_status tile_fault(unsigned int* fault, int clear) {
+  cudaError_t err = cudaMemcpyFromSymbol(fault, g_tile_fault, sizeof(unsigned int));
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (clear) {
+    const unsigned int zero = 0;
+    err = cudaMemcpyToSymbol(g_tile_fault, &zero, sizeof(unsigned int));
+    if (err != cudaSuccess) return cuda_fail(err);
+  }
+  return TK_OK;
+}
+
+}  // namespace tk_internal
+
+extern "C" {
+
+size_t tk_per_channel_workspace_bytes(int64_t K) {
+  if (K <= 0 || K > (int64_t(1) << 28)) return 0;
+  const int64_t k_pad = (K + kTileCols - 1) / kTileCols * kTileCols;
+  return (size_t)(12 * k_pad);
+}
+
+tk_status tk_per_block_cast(const void* x, int64_t M, int64_t K, int64_t ld_x, int fmt,
+                            int mode, void* codes, int64_t ld_codes, void* scales,
+                            int64_t ld_scales, void* stream) {
+  tk_status st = check_tile_args(M, K, ld_x, fmt, mode, ld_codes);
+  if (st != TK_OK) return st;
+  const int64_t n_cb = (K + kTileCols - 1) / kTileCols;
+  const int64_t words = mode == TK_SCALE_UE8M0_PACKED ? (n_cb + 3) / 4 : n_cb;
+  if (ld_scales < words) return TK_ERR_INVALID_ARG;
+  if (M == 0) return TK_OK;
+  st = check_tile_pointers(x, ld_x, codes, ld_codes, scales);
+  if (st != TK_OK) return st;
+  const int64_t n_tiles = (M + kTileRows - 1) / kTileRows * n_cb;
+  if (n_tiles > INT32_MAX) return TK_ERR_UNSUPPORTED;
+
+  TileParams p = base_params(M, K, mode, codes, ld_codes, scales);
+  p.ld_scales = ld_scales;
+  p.n_tiles = (int)n_tiles;
+  CUtensorMap map;
+  st = make_map(&map, x, M, K, ld_x);
+  if (st != TK_OK) return st;
+  return launch_tile(pick_tile<kBlockCast>(fmt, mode != TK_SCALE_FP32), map, p, stream);
+}
+
+tk_status tk_per_channel_cast(const void* x, int64_t M, int64_t K, int64_t ld_x, int fmt,
+                              int mode, void* codes, int64_t ld_codes, void* scales,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  tk_status st = check_tile_args(M, K, ld_x, fmt, mode, ld_codes);
+  if (st != TK_OK) return st;
+  if (workspace_bytes < tk_per_channel_workspace_bytes(K)) return TK_ERR_INVALID_ARG;
+  if (M == 0) return TK_OK;
+  st = check_tile_pointers(x, ld_x, codes, ld_codes, scales);
+  if (st != TK_OK) return st;
+  if (workspace == nullptr) return TK_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return TK_ERR_MISALIGNED;
+  const int64_t n_tiles = (M + kTileRows - 1) / kTileRows * ((K + kTileCols - 1) / kTileCols);
+  if (n_tiles > INT32_MAX) return TK_ERR_UNSUPPORTED;
+
+  TileParams p = base_params(M, K, mode, codes, ld_codes, scales);
+  p.n_tiles = (int)n_tiles;
+  p.col_amax = static_cast<unsigned int*>(workspace);
+  p.col_s = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 4 * (size_t)p.k_pad);
+  CUtensorMap map;
+  st = make_map(&map, x, M, K, ld_x);
+  if (st != TK_OK) return st;
+  const bool pow2 = mode != TK_SCALE_FP32;
+
+  // 0. column maxima start at +0 (the bit pattern 0)
+  cudaError_t err = cudaMemsetAsync(p.col_amax, 0, 4 * (size_t)p.k_pad,
+                                    static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err);
+  // 1. column amax
+  st = launch_tile(tile_cast_kernel<TK_FMT_E4M3, false, kColumnAmax>, map, p, stream);
+  if (st != TK_OK) return st;
+  // 2. column scales
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg =
+      dependent_launch(attr, (unsigned)((p.k_pad + 255) / 256), 256, 0, stream);
+  err = cudaLaunchKernelEx(&cfg, pick_scale(fmt, pow2), p);
+  if (err == cudaSuccess) err = cudaGetLastError();
+  if (err != cudaSuccess) return cuda_fail(err);
+  // 3. cast
+  return launch_tile(pick_tile<kChannelCast>(fmt, pow2), map, p, stream);
+}
+
+}  // extern "C"

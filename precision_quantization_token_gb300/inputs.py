@@ -19,6 +19,8 @@ Workloads are the shapes and value mixes the per-token cast is measured on:
        field 0, mantissa uniform in 1..127, random sign)
   d2   dequantization of c2's codes and scales to BF16 (4096 x 7168)
   b2   cast-and-cast-back of c2's input (4096 x 7168, E4M3 g128 UE8M0)
+  pb2  per-block cast (128 x 128 blocks) of c2's input, E4M3, fp32 scales
+  pc2  per-channel cast (one scale per column) of c2's input, E4M3, fp32
 
 Random draws use numpy's PCG64 generator seeded per workload; fp32 values are
 rounded to BF16 with round-to-nearest-even on the bit pattern.
@@ -45,6 +47,7 @@ class Workload:
     seed: int
     dist: str
     op: str = "cast"   # "cast" | "swiglu" | "dequant" | "cast_back"
+    #                  | "block" | "channel"
 
     @property
     def in_cols(self) -> int:
@@ -68,11 +71,28 @@ class Workload:
         if self.op == "cast_back":
             read = self.M * self.K * 2
             return {"read": read, "bf16_out": read, "total": 2 * read}
+        if self.op in ("block", "channel"):
+            if self.op == "block":
+                n = -(-self.K // 128)
+                rows = -(-self.M // 128)
+            else:
+                n, rows = self.K, 1
+            words = (n + 3) // 4 if self.scale == "ue8m0" else n
+            scales = rows * words * 4
+            read = self.M * self.K * 2
+            return {"read": read, "codes": codes, "scales": scales,
+                    "total": read + codes + scales}
         read = self.M * self.in_cols * 2
         return {"read": read, "codes": codes, "scales": scales,
                 "total": read + codes + scales}
 
     def describe(self) -> str:
+        if self.op == "block":
+            return (f"per_block_cast {self.fmt.upper()} 128x128 blocks "
+                    f"{self.scale} {self.M}x{self.K} ({self.dist})")
+        if self.op == "channel":
+            return (f"per_channel_cast {self.fmt.upper()} {self.scale} "
+                    f"{self.M}x{self.K} ({self.dist})")
         op = {"cast": "per_token_cast", "swiglu": "swiglu_per_token_cast",
               "dequant": "per_token_dequant",
               "cast_back": "per_token_cast_back"}[self.op]
@@ -99,6 +119,10 @@ WORKLOADS = {
                    "normal, 0.1% x100 outliers", op="dequant"),
     "b2": Workload("b2", 4096, 7168, 128, "e4m3", "ue8m0", "row", False, 2,
                    "normal, 0.1% x100 outliers", op="cast_back"),
+    "pb2": Workload("pb2", 4096, 7168, 128, "e4m3", "fp32", "row", False, 2,
+                    "normal, 0.1% x100 outliers", op="block"),
+    "pc2": Workload("pc2", 4096, 7168, 4096, "e4m3", "fp32", "row", False, 2,
+                    "normal, 0.1% x100 outliers", op="channel"),
 }
 
 

@@ -33,6 +33,7 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert "tk_per_token_cast" in names and "tk_swiglu_per_token_cast" in names
+    assert "tk_per_block_cast" in names and "tk_per_channel_cast" in names
     raw = ctypes.CDLL(tk.library_path())
     for n in names:
         assert hasattr(raw, n), n
@@ -143,7 +144,88 @@ def test_cast_back_validation(lib, name, kw, want):
     assert call_cb(lib, **kw) == want
 
 
+def call_pb(lib, *, x=A, M=4, K=256, ld_x=256, fmt=0, mode=0, codes=B,
+            ld_codes=256, scales=C, ld_scales=2):
+    return lib.tk_per_block_cast(x, M, K, ld_x, fmt, mode, codes, ld_codes,
+                                 scales, ld_scales, None)
+
+
+PB_CASES = [
+    ("bad fmt", dict(fmt=2), INVALID),
+    ("bad mode", dict(mode=3), INVALID),
+    ("K not multiple of 16", dict(K=200, ld_x=256), INVALID),
+    ("K zero", dict(K=0), INVALID),
+    ("negative M", dict(M=-1), INVALID),
+    ("ld_x < K", dict(ld_x=128), INVALID),
+    ("ld_codes < K", dict(ld_codes=128), INVALID),
+    ("e2m1 ld_codes < K/2", dict(fmt=1, ld_codes=112), INVALID),
+    ("scale row too narrow", dict(ld_scales=1), INVALID),
+    ("ragged K needs another word", dict(K=272, ld_x=272, ld_codes=272,
+                                         ld_scales=2), INVALID),
+    ("packed scale row too narrow", dict(mode=2, K=1280, ld_x=1280,
+                                         ld_codes=1280, ld_scales=2), INVALID),
+    ("null x", dict(x=None), INVALID),
+    ("null codes", dict(codes=None), INVALID),
+    ("null scales", dict(scales=None), INVALID),
+    ("x misaligned", dict(x=A + 8), MISALIGNED),
+    ("ld_x not 16 bytes", dict(K=128, ld_x=132, ld_scales=1), MISALIGNED),
+    ("codes misaligned", dict(codes=B + 4), MISALIGNED),
+    ("ld_codes not 16", dict(ld_codes=264), MISALIGNED),
+    ("scales misaligned", dict(scales=C + 2), MISALIGNED),
+    ("M too large", dict(M=(1 << 30) + 1), UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", PB_CASES, ids=[c[0] for c in PB_CASES])
+def test_per_block_validation(lib, name, kw, want):
+    assert call_pb(lib, **kw) == want
+
+
+WS = 0x40000
+
+
+def call_pc(lib, *, x=A, M=4, K=256, ld_x=256, fmt=0, mode=0, codes=B,
+            ld_codes=256, scales=C, ws=WS, ws_bytes=12 * 256):
+    return lib.tk_per_channel_cast(x, M, K, ld_x, fmt, mode, codes, ld_codes,
+                                   scales, ws, ws_bytes, None)
+
+
+PC_CASES = [
+    ("bad fmt", dict(fmt=2), INVALID),
+    ("bad mode", dict(mode=7), INVALID),
+    ("K not multiple of 16", dict(K=120, ld_x=128), INVALID),
+    ("ld_x < K", dict(ld_x=128), INVALID),
+    ("ld_codes < K", dict(ld_codes=128), INVALID),
+    ("workspace too small", dict(ws_bytes=12 * 256 - 1), INVALID),
+    ("workspace for padded K", dict(K=272, ld_x=272, ld_codes=272,
+                                    ws_bytes=12 * 272), INVALID),
+    ("null workspace", dict(ws=None), INVALID),
+    ("null x", dict(x=None), INVALID),
+    ("null scales", dict(scales=None), INVALID),
+    ("workspace misaligned", dict(ws=WS + 8), MISALIGNED),
+    ("x misaligned", dict(x=A + 8), MISALIGNED),
+    ("scales misaligned", dict(scales=C + 1), MISALIGNED),
+    ("K too large", dict(K=(1 << 28) + 16, ld_x=(1 << 28) + 16,
+                         ld_codes=(1 << 28) + 16, ws_bytes=1 << 40), UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", PC_CASES, ids=[c[0] for c in PC_CASES])
+def test_per_channel_validation(lib, name, kw, want):
+    assert call_pc(lib, **kw) == want
+
+
+def test_per_channel_workspace_size(lib):
+    assert tk.tk_per_channel_workspace_bytes(256) == 12 * 256
+    assert tk.tk_per_channel_workspace_bytes(16) == 12 * 128
+    assert tk.tk_per_channel_workspace_bytes(7168) == 12 * 7168
+    assert tk.tk_per_channel_workspace_bytes(0) == 0
+    assert tk.tk_per_channel_workspace_bytes(-5) == 0
+
+
 def test_empty_batch_is_a_noop(lib):
+    assert call_pb(lib, M=0, x=None, codes=None, scales=None) == OK
+    assert call_pc(lib, M=0, x=None, codes=None, scales=None, ws=None) == OK
     assert call_dq(lib, M=0, codes=None, scales=None, y=None) == OK
     assert call_cb(lib, M=0, x=None, y=None) == OK
     assert call(lib, M=0, x=None, codes=None, scales=None) == OK

@@ -1,0 +1,254 @@
+"""Parity of the per-block and per-channel casts with the oracle (GPU).
+
+The CUDA path is called through the C ABI on guard-banded buffers (a
+sentinel row above and below the codes and the scales, sentinel stride
+padding, a poisoned input stride pad); the oracle runs on the same host
+bytes; codes, scales and every sentinel must agree bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import precision_quantization_token_gb300 as tk
+from gpu_util import FMT_ID, MODE_ID, THREADS, torch_mod
+from precision_quantization_token_gb300.inputs import (WORKLOADS, make_input,
+                                                       random_bf16)
+
+pytestmark = pytest.mark.gpu
+
+SENT_CODE = 0xA5
+SENT_WORD = 0x5A5A5A5A
+POISON_BF16 = 0x7F00
+FMTS = ["e4m3", "e2m1"]
+MODES = ["fp32", "pow2", "ue8m0"]
+
+
+def _host_x(bits, ld_x):
+    M, K = bits.shape
+    x = np.full((M, ld_x), POISON_BF16, np.uint16)
+    x[:, :K] = bits
+    return x
+
+
+def _stream():
+    return torch_mod().cuda.current_stream().cuda_stream
+
+
+def _dev(a, dtype_view=None):
+    torch = torch_mod()
+    return torch.from_numpy(a.view(dtype_view) if dtype_view else a).cuda()
+
+
+def _row_bytes(K, fmt):
+    return K if fmt == "e4m3" else K // 2
+
+
+def run_block(bits, fmt, mode, ld_x=None, code_pad=0, scale_pad=0):
+    """(gpu codes, gpu scales, oracle codes, oracle scales), guards included."""
+    torch = torch_mod()
+    M, K = bits.shape
+    ld_x = ld_x or K
+    x = _host_x(bits, ld_x)
+    rb = _row_bytes(K, fmt)
+    ld_codes = (rb + code_pad + 15) // 16 * 16
+    nr, nw, _ = oracle.block_scale_shape(M, K, 128, MODE_ID[mode])
+    ld_s = nw + scale_pad
+    codes = np.full((M + 2, ld_codes), SENT_CODE, np.uint8)
+    scales = np.full((nr + 2, ld_s), SENT_WORD, np.uint32)
+
+    xd, cd, sd = _dev(x, np.int16), _dev(codes), _dev(scales, np.int32)
+    tk.tk_per_block_cast(xd.data_ptr(), M, K, ld_x, tk.FMT[fmt],
+                         tk.SCALE[mode], cd.data_ptr() + ld_codes, ld_codes,
+                         sd.data_ptr() + 4 * ld_s, ld_s, _stream())
+    torch.cuda.synchronize()
+    gc, gs = cd.cpu().numpy(), sd.cpu().numpy().view(np.uint32)
+
+    rc, rs = codes.copy(), scales.copy()
+    s_view = rs[1:nr + 1].view(np.int32 if mode == "ue8m0" else np.float32)
+    if M:
+        oracle.per_block_cast(x, K, 128, FMT_ID[fmt], MODE_ID[mode],
+                              codes=rc[1:M + 1], scales=s_view,
+                              threads=THREADS)
+    return gc, gs, rc, rs
+
+
+def run_channel(bits, fmt, mode, ld_x=None, code_pad=0, workspace=None):
+    torch = torch_mod()
+    M, K = bits.shape
+    ld_x = ld_x or K
+    x = _host_x(bits, ld_x)
+    rb = _row_bytes(K, fmt)
+    ld_codes = (rb + code_pad + 15) // 16 * 16
+    nw, _ = oracle.channel_scale_shape(K, MODE_ID[mode])
+    codes = np.full((M + 2, ld_codes), SENT_CODE, np.uint8)
+    scales = np.full(nw + 8, SENT_WORD, np.uint32)      # 4 guard words each side
+
+    xd, cd, sd = _dev(x, np.int16), _dev(codes), _dev(scales, np.int32)
+    need = tk.tk_per_channel_workspace_bytes(K)
+    if workspace is None:     # contents on entry must not matter: fill with junk
+        workspace = torch.full((need,), 0xEE, dtype=torch.uint8, device="cuda")
+    tk.tk_per_channel_cast(xd.data_ptr(), M, K, ld_x, tk.FMT[fmt],
+                           tk.SCALE[mode], cd.data_ptr() + ld_codes, ld_codes,
+                           sd.data_ptr() + 16, workspace.data_ptr(),
+                           workspace.numel(), _stream())
+    torch.cuda.synchronize()
+    gc, gs = cd.cpu().numpy(), sd.cpu().numpy().view(np.uint32)
+
+    rc, rs = codes.copy(), scales.copy()
+    s_view = rs[4:4 + nw].view(np.int32 if mode == "ue8m0" else np.float32)
+    if M:
+        oracle.per_channel_cast(x, K, FMT_ID[fmt], MODE_ID[mode],
+                                codes=rc[1:M + 1], scales=s_view,
+                                threads=THREADS)
+    return gc, gs, rc, rs
+
+
+def assert_same(gc, gs, rc, rs):
+    if not np.array_equal(gc, rc):
+        bad = np.argwhere(gc != rc)
+        r, c = bad[0]
+        raise AssertionError(f"codes differ at {bad.shape[0]} bytes; first "
+                             f"(row {r - 1}, byte {c}): gpu {gc[r, c]:#04x} "
+                             f"oracle {rc[r, c]:#04x}")
+    if not np.array_equal(gs, rs):
+        bad = np.argwhere(gs != rs)
+        raise AssertionError(f"scales differ at {bad.shape[0]} words; first "
+                             f"{bad[0]}: gpu {gs[tuple(bad[0])]:#010x} oracle "
+                             f"{rs[tuple(bad[0])]:#010x}")
+
+
+def bits_with_specials(M, K, seed):
+    """Normal values spread over rows and columns, plus exact zero blocks /
+    columns, -0, BF16 denormals and the BF16 maximum."""
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((M, K)).astype(np.float32)
+    v *= np.exp2(rng.integers(-8, 9, (M, 1))).astype(np.float32)
+    v *= np.exp2(rng.integers(-6, 7, (1, K))).astype(np.float32)
+    bits = (v.view(np.uint32) >> 16).astype(np.uint16)
+    bits[rng.random((M, K)) < 0.02] = 0x8000                   # -0
+    den = rng.random((M, K)) < 0.01
+    bits[den] = (rng.integers(1, 128, den.sum()) |
+                 (rng.integers(0, 2, den.sum()) << 15)).astype(np.uint16)
+    if M > 130 and K > 140:
+        bits[:128, :128] = 0                                   # a zero block
+        bits[128:, 3] = 0                                      # zero column tail
+        bits[129, 137] = 0x7F7F                                # BF16 max
+        bits[130, 138] = 0xFF7F                                # -BF16 max
+    return bits
+
+
+# ---------------------------------------------------------------- full size
+
+@pytest.mark.parametrize("name", ["pb2", "pc2"])
+def test_full_workload(name):
+    w = WORKLOADS[name]
+    bits = make_input(w)
+    run = run_block if w.op == "block" else run_channel
+    assert_same(*run(bits, w.fmt, w.scale))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("mode", MODES)
+def test_full_shape_every_option(fmt, mode):
+    bits = make_input(WORKLOADS["c2"], M=1024)
+    assert_same(*run_block(bits, fmt, mode))
+    assert_same(*run_channel(bits, fmt, mode))
+
+
+# ------------------------------------------------------------------ shapes
+
+SHAPES = [(1, 16), (1, 128), (127, 128), (128, 256), (129, 272), (300, 400),
+          (255, 2064), (640, 7184), (2, 4096)]
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("mode", MODES)
+def test_block_shapes(M, K, fmt, mode):
+    assert_same(*run_block(bits_with_specials(M, K, seed=M * 7 + K), fmt, mode))
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("mode", MODES)
+def test_channel_shapes(M, K, fmt, mode):
+    assert_same(*run_channel(bits_with_specials(M, K, seed=M * 5 + K), fmt,
+                             mode))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_strides_and_pads(fmt):
+    bits = bits_with_specials(300, 400, seed=3)
+    assert_same(*run_block(bits, fmt, "ue8m0", ld_x=424, code_pad=32,
+                           scale_pad=3))
+    assert_same(*run_block(bits, fmt, "fp32", ld_x=408, code_pad=16,
+                           scale_pad=1))
+    assert_same(*run_channel(bits, fmt, "fp32", ld_x=416, code_pad=48))
+
+
+def test_tall_columns():
+    """Many row tiles fold into each column amax (atomics across CTAs)."""
+    bits = random_bf16(8, 70000, 48)
+    bits[69999, 5] = 0x4600                                    # lone max, last row
+    bits[0, 6] = 0xC600                                        # lone -max, first row
+    for mode in MODES:
+        assert_same(*run_channel(bits, "e4m3", mode))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_every_bf16_value(fmt):
+    """All 65,280 finite BF16 patterns (a 256 x 256 matrix with the NaN/Inf
+    patterns replaced by zero): every value passes through both casts."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    exp = (bits >> 7) & 0xFF
+    bits[exp == 0xFF] = 0
+    bits = bits.reshape(256, 256)
+    for mode in MODES:
+        assert_same(*run_block(bits, fmt, mode))
+        assert_same(*run_channel(bits, fmt, mode))
+        assert_same(*run_channel(np.ascontiguousarray(bits.T), fmt, mode))
+
+
+def test_workspace_reused_across_calls():
+    """Two calls in a row on one workspace: the second does not see the
+    first's column maxima."""
+    torch = torch_mod()
+    ws = torch.empty(tk.tk_per_channel_workspace_bytes(512), dtype=torch.uint8,
+                     device="cuda")
+    big = random_bf16(1, 200, 512, scale=100.0)
+    small = random_bf16(2, 200, 512, scale=0.01)
+    assert_same(*run_channel(big, "e4m3", "fp32", workspace=ws))
+    assert_same(*run_channel(small, "e4m3", "fp32", workspace=ws))
+
+
+def test_empty_batch_is_a_noop():
+    torch = torch_mod()
+    s = _stream()
+    tk.tk_per_block_cast(0, 0, 256, 256, 0, 0, 0, 256, 0, 2, s)
+    tk.tk_per_channel_cast(0, 0, 256, 256, 0, 0, 0, 256, 0, 0,
+                           tk.tk_per_channel_workspace_bytes(256), s)
+    torch.cuda.synchronize()
+
+
+def test_tensor_api():
+    torch = torch_mod()
+    bits = make_input(WORKLOADS["c2"], M=512)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    for fmt in FMTS:
+        for mode in MODES:
+            c, s = tk.per_block_cast(x, fmt, mode)
+            rc, rs = oracle.per_block_cast(bits, 7168, 128, FMT_ID[fmt],
+                                           MODE_ID[mode], threads=THREADS)
+            assert np.array_equal(c.cpu().numpy(), rc)
+            assert np.array_equal(s.cpu().numpy().view(np.uint32),
+                                  rs.view(np.uint32))
+            c, s = tk.per_channel_cast(x, fmt, mode)
+            rc, rs = oracle.per_channel_cast(bits, 7168, FMT_ID[fmt],
+                                             MODE_ID[mode], threads=THREADS)
+            assert np.array_equal(c.cpu().numpy(), rc)
+            assert np.array_equal(s.cpu().numpy().view(np.uint32),
+                                  rs.view(np.uint32))
+
+
+def test_zz_no_tile_kernel_gave_up_on_a_wait():
+    assert tk.tk_get_device_fault(clear=False) == 0

@@ -7,7 +7,8 @@ per format).
 
 IEEE fp32 multiply, FMA and division round identically on the host and the
 GPU (no flush to zero on either side), so the host enumeration proves the
-device arithmetic.  The CUDA source is checked to still use that sequence.
+device arithmetic.  The CUDA source (the quotient step every cast kernel
+shares) is checked to still use that sequence.
 """
 import os
 import platform
@@ -20,7 +21,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "quotient_check.c")
 CU = os.path.join(ROOT, "precision_quantization_token_gb300", "csrc",
-                  "tk_cast.cu")
+                  "tk_device.cuh")
 
 
 def _has_fma_flag():
