@@ -229,7 +229,14 @@ class GpuWorkload:
         bits = make_input(w)
         x0 = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
         row_bytes = w.K if w.fmt == "e4m3" else w.K // 2
-        shape, dt = tk.scale_shape(w.M, w.K, w.group, w.scale, w.layout)
+        if w.op == "block":
+            shape, dt = tk.block_scale_shape(w.M, w.K, w.scale)
+        elif w.op == "channel":
+            shape, dt = tk.channel_scale_shape(w.K, w.scale)
+            self.workspace = torch.zeros(tk.tk_per_channel_workspace_bytes(w.K),
+                                         dtype=torch.uint8, device=device)
+        else:
+            shape, dt = tk.scale_shape(w.M, w.K, w.group, w.scale, w.layout)
         if w.op == "dequant":
             # the codes and scales to dequantize come from one (untimed) cast
             c0, s0 = tk.per_token_cast(x0, w.group, w.fmt, w.scale, w.layout)
@@ -269,6 +276,17 @@ class GpuWorkload:
                                       w.group, tk.FMT[w.fmt],
                                       tk.SCALE[w.scale], b.data_ptr(),
                                       b.stride(0), stream_handle)
+        elif w.op == "block":
+            tk.tk_per_block_cast(a.data_ptr(), w.M, w.K, a.stride(0),
+                                 tk.FMT[w.fmt], tk.SCALE[w.scale],
+                                 b.data_ptr(), b.stride(0), c.data_ptr(),
+                                 c.stride(0), stream_handle)
+        elif w.op == "channel":
+            tk.tk_per_channel_cast(a.data_ptr(), w.M, w.K, a.stride(0),
+                                   tk.FMT[w.fmt], tk.SCALE[w.scale],
+                                   b.data_ptr(), b.stride(0), c.data_ptr(),
+                                   self.workspace.data_ptr(),
+                                   self.workspace.numel(), stream_handle)
         else:
             self.entry(a.data_ptr(), w.M, w.K, a.stride(0), w.group,
                        tk.FMT[w.fmt], tk.SCALE[w.scale], tk.LAYOUT[w.layout],
@@ -424,6 +442,7 @@ def run_gpu(args):
                               max(3, args.warmup), fw, fr, 1)
             gbps = other.bytes["total"] / (m * 1e-3) / 1e9
             table[name] = {"workload": other.w.describe(),
+                           "kernels_per_step": 2 if other.w.op == "channel" else 1,
                            "ms": round(m, 6), "GB/s": round(gbps, 1),
                            "frac_of_peak": round(gbps / peak, 4),
                            "bytes": other.bytes["total"],

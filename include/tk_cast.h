@@ -208,8 +208,9 @@ TK_API tk_status tk_per_block_cast(const void *x, int64_t M, int64_t K,
                                    void *scales, int64_t ld_scales,
                                    void *stream);
 
-/* Bytes of workspace tk_per_channel_cast needs for K channels: 12 per
- * channel, K rounded up to a multiple of TK_BLOCK (0 if K is out of range). */
+/* Bytes of workspace tk_per_channel_cast needs for K channels: 4 per
+ * channel with K rounded up to a multiple of TK_BLOCK, plus 4 per TK_BLOCK
+ * channels rounded up to 16 (0 if K is out of range). */
 TK_API size_t tk_per_channel_workspace_bytes(int64_t K);
 
 /*
@@ -223,12 +224,16 @@ TK_API size_t tk_per_channel_workspace_bytes(int64_t K);
  *             UE8M0 bytes (channel k in byte k % 4 of word k / 4).  4-byte
  *             aligned.
  *   workspace device memory of at least tk_per_channel_workspace_bytes(K)
- *             bytes, 16-byte aligned, owned by the caller.  Its contents on
- *             entry do not matter; the call overwrites them (column maxima,
- *             scales and their reciprocals).  Calls that may run at the same
- *             time (other streams) must not share a workspace.
- *   Enqueues on `stream` a memset of the workspace's column maxima and
- *   three kernels (column amax, column scales, cast); x is read twice.
+ *             bytes, 16-byte aligned, owned by the caller, ZERO-FILLED
+ *             before its first use (e.g. one cudaMemset).  It holds the
+ *             column maxima and per-strip counters during the call, and
+ *             every call that completes leaves it zero-filled again, so one
+ *             workspace serves any sequence of calls on one stream.  Calls
+ *             that may run at the same time (other streams) must not share
+ *             a workspace.  If tk_get_device_fault reports a fault, zero it
+ *             again before the next call.
+ *   Enqueues two kernels on `stream` (column amax, then the cast, which
+ *   derives each column's scale from its maximum); x is read twice.
  *   M == 0 writes nothing (no element to take a scale from).
  */
 TK_API tk_status tk_per_channel_cast(const void *x, int64_t M, int64_t K,

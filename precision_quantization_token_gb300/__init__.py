@@ -369,13 +369,37 @@ def per_block_cast(x, fmt: str = "e4m3", scale: str = "fp32", *, codes=None,
     return codes, scales
 
 
+_workspaces = {}
+
+
+def channel_workspace(K: int, device=None, stream=None):
+    """A zero-filled per-channel workspace of at least
+    ``tk_per_channel_workspace_bytes(K)`` bytes, kept per (device, stream):
+    every completed call leaves it zero-filled, so calls issued on one
+    stream can share it (calls on different streams get different ones)."""
+    import torch
+    dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    need = max(16, tk_per_channel_workspace_bytes(K))
+    key = (dev.index, stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
 def per_channel_cast(x, fmt: str = "e4m3", scale: str = "fp32", *,
                      codes=None, scales=None, workspace=None, stream=None):
     """Per-channel cast of a bfloat16 [M, K] CUDA tensor: one scale per
     column over all rows.  Returns (codes, scale vector, see
-    ``channel_scale_shape``).  ``workspace`` (uint8 CUDA tensor of at least
-    ``tk_per_channel_workspace_bytes(K)`` bytes) is allocated per call when
-    not given; calls in flight together must not share one."""
+    ``channel_scale_shape``).  ``workspace`` (a zero-filled uint8 CUDA
+    tensor of at least ``tk_per_channel_workspace_bytes(K)`` bytes, left
+    zero-filled by the call) defaults to ``channel_workspace`` for the
+    call's device and stream."""
     import torch
     _check_x(x)
     M, K = x.shape
@@ -383,12 +407,10 @@ def per_channel_cast(x, fmt: str = "e4m3", scale: str = "fp32", *,
     if scales is None:
         shape, dt = channel_scale_shape(K, scale)
         scales = torch.empty(shape, dtype=getattr(torch, dt), device=x.device)
-    need = tk_per_channel_workspace_bytes(K)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8,
-                                device=x.device)
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
+    if workspace is None:
+        workspace = channel_workspace(K, x.device, stream)
     tk_per_channel_cast(x.data_ptr(), M, K, x.stride(0), FMT[fmt],
                         SCALE[scale], codes.data_ptr(), codes.stride(0),
                         scales.data_ptr(), workspace.data_ptr(),

@@ -27,19 +27,27 @@
 //    into registers and releases the stage at once, reduces its amax by
 //    shuffles, and the group combines its 8 warp maxima in shared memory
 //    behind a named barrier; every warp then casts from registers.
-//  * Per-channel cast: after the caller's workspace of column maxima is
-//    cleared, three launches:
+//  * Per-channel cast, two launches on a caller workspace that holds the
+//    column maxima and one counter per 128-channel strip, all zero between
+//    calls:
 //      1. column amax: per tile, each group reduces the 128 column maxima of
 //         its 128 rows in shared memory and folds them into the workspace
 //         with atomicMax on the fp32 bit patterns (non-negative floats order
 //         like their bit patterns; max is exact and order-independent, so
-//         the result does not depend on timing);
-//      2. column scales: one thread per channel computes s and its
-//         reciprocal into the workspace and writes the caller's scale vector;
-//      3. cast: the tile pipeline again, each lane dividing its 8 channels
-//         by their own scales.
-//    Launches 1-3 are programmatic dependents: each waits
-//    (griddepcontrol.wait) for its predecessor before touching memory.
+//         the result does not depend on timing).  Its tile loads ask L2 to
+//         keep the input (evict_last) for the second read;
+//      2. cast: the tile pipeline again; with each tile the producer also
+//         copies the tile's 128 column maxima (512 bytes) into the stage, the
+//         group turns them into 128 scales and reciprocals in shared memory,
+//         and each lane divides its 8 channels by their own scales.  The
+//         tiles of the first block row write the caller's scale vector.
+//         Each tile then counts itself in its strip's counter; the tile that
+//         completes the count (every copy of the strip's maxima has landed)
+//         sets the strip's maxima and counter back to zero, so the next call
+//         needs no clearing pass (a memset between the launches would cost
+//         a serialised gap of several microseconds).
+//    Launch 2 is a programmatic dependent: it waits (griddepcontrol.wait)
+//    for launch 1 before touching memory.
 //  * Every wait is bounded in time; on expiry the kernel records a fault
 //    code (tk_get_device_fault), stops, lets its own copies land and
 //    returns.  The groups agree on stopping through a barrier reduction, so
@@ -66,21 +74,26 @@ constexpr int kTileCols = TK_BLOCK;                 // channels per tile (256 B 
 constexpr int kTileRows = TK_BLOCK;                 // rows per tile (the block height)
 constexpr int kRowBytes = kTileCols * 2;
 constexpr int kTileBytes = kTileRows * kRowBytes;  // 32 KiB
+constexpr int kAmaxBytes = kTileCols * 4;           // per-channel: the tile's column maxima
+constexpr int kStageBytes = kTileBytes + kAmaxBytes;
+static_assert(kStageBytes % 128 == 0, "tensor copies need 128-byte aligned stages");
 constexpr int kGroupWarps = 8;
 constexpr int kGroups = 3;
 constexpr int kStages = 6;
 constexpr int kConsumerWarps = kGroups * kGroupWarps;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kPrefetchTiles = 2;
+constexpr int kPrefetchTiles = 4;
+constexpr int kCtasPerSm = 1;
 constexpr int kWarpRows = kTileRows / kGroupWarps;    // 16
 constexpr int kSteps = kWarpRows / 2;                 // 2 rows per warp step
 static_assert(kStages % kGroups == 0, "each stage belongs to one group");
 static_assert(kTileCols == 16 * 8, "16 lanes x 8 channels cover a tile row");
 
-// Shared memory, from a 1024-byte aligned base: the ring, the full and empty
-// mbarriers, an abort flag, and per group two buffers of 8 x 128 floats for
-// the cross-warp reductions.
-constexpr int kBarOffset = kStages * kTileBytes;
+// Shared memory, from a 1024-byte aligned base: the ring (each stage a tile
+// plus a slot for its column maxima), the full and empty mbarriers, an abort
+// flag, and per group two buffers of 8 x 128 floats for the cross-warp
+// reductions (the per-channel cast keeps 128 scales and reciprocals there).
+constexpr int kBarOffset = kStages * kStageBytes;
 constexpr int kFlagOffset = kBarOffset + 16 * kStages;
 constexpr int kRedOffset = kFlagOffset + 16;
 constexpr int kRedFloats = 2 * kGroupWarps * kTileCols;   // per group
@@ -100,9 +113,10 @@ struct TileParams {
   uint8_t* scales;           // block: 4-byte words, block row rb at rb * ld_scales
   int64_t ld_scales;         //   words; channel: a vector of K entries
   unsigned int* col_amax;    // channel: [k_pad] fp32 bit patterns
-  float* col_s;              // channel: [k_pad] scales then [k_pad] reciprocals
+  unsigned int* strip_count; // channel: [n_cb] tiles of each strip cast so far
   int M, K;
   int n_cb;                  // tile (block) columns: ceil(K / 128)
+  int n_rb;                  // tile (block) rows: ceil(M / 128)
   int n_tiles;
   int k_pad;                 // n_cb * 128
   int ue8m0;                 // 1: packed exponent bytes, 0: fp32 words
@@ -110,12 +124,25 @@ struct TileParams {
 
 // ------------------------------------------------------------ primitives
 
+// L2 eviction priority of a kernel's tile loads (a hint; no effect on values).
+template <int OP>
+__device__ __forceinline__ uint64_t load_policy() {
+  uint64_t pol;
+  if constexpr (OP == kColumnAmax)        // read again by the cast: keep it
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  else if constexpr (OP == kChannelCast)  // second read, mostly from L2
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  else                                    // read once
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map,
-                                            int c, int r, uint32_t bar) {
+                                            int c, int r, uint32_t bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(r), "r"(bar), "l"(pol)
       : "memory");
 }
 
@@ -176,6 +203,7 @@ __device__ __forceinline__ uint8_t* code_ptr(const TileParams& p, int row, int c
 
 // ------------------------------------------------------------ producer
 
+template <int OP>
 __device__ void tile_produce(const CUtensorMap* map, const TileParams& p,
                              uint32_t ring, uint32_t full0, uint32_t empty0,
                              volatile int* abort_flag, int my_tiles) {
@@ -191,6 +219,7 @@ __device__ void tile_produce(const CUtensorMap* map, const TileParams& p,
     tma_prefetch_2d(map, (t - rb * p.n_cb) * kTileCols, rb * kTileRows);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint64_t pol = load_policy<OP>();
   int issued = 0;
   for (int i = 0; i < my_tiles; ++i) {
     const int s = i % kStages;
@@ -203,10 +232,14 @@ __device__ void tile_produce(const CUtensorMap* map, const TileParams& p,
     if (*abort_flag) break;
     const int t = (int)blockIdx.x + i * (int)gridDim.x;
     const int rb = t / p.n_cb;
+    const int cb = t - rb * p.n_cb;
     const uint32_t full = full0 + 8 * s;
-    mbar_arrive_expect_tx(full, kTileBytes);   // the whole box, zero fill included
-    tma_load_2d(ring + (uint32_t)(s * kTileBytes), map, (t - rb * p.n_cb) * kTileCols,
-                rb * kTileRows, full);
+    const uint32_t dst = ring + (uint32_t)(s * kStageBytes);
+    // the whole box counts, zero fill included
+    mbar_arrive_expect_tx(full, OP == kChannelCast ? kStageBytes : kTileBytes);
+    tma_load_2d(dst, map, cb * kTileCols, rb * kTileRows, full, pol);
+    if constexpr (OP == kChannelCast)   // the tile's 128 column maxima (k_pad covers them)
+      bulk_load(dst + kTileBytes, p.col_amax + cb * kTileCols, kAmaxBytes, full);
     issued = i + 1;
   }
   // Let every copy this thread issued land before the CTA can exit.
@@ -222,7 +255,7 @@ __device__ void tile_produce(const CUtensorMap* map, const TileParams& p,
 // ------------------------------------------------------------ the kernel
 
 template <int FMT, bool POW2, int OP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -247,7 +280,7 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
 
   const int my_tiles = (p.n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
   if (warp == kConsumerWarps) {
-    if (lane == 0) tile_produce(&map, p, base, full0, empty0, abort_flag, my_tiles);
+    if (lane == 0) tile_produce<OP>(&map, p, base, full0, empty0, abort_flag, my_tiles);
     return;
   }
 
@@ -271,16 +304,41 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
     const int r0 = rb * kTileRows + gw * kWarpRows + half;   // this lane's first row
     const int col = cb * kTileCols + chunk * 8;               // this lane's first channel
 
+    const uint32_t stage = base + (uint32_t)(s * kStageBytes);
+    float* buf = red + (n & 1) * (kGroupWarps * kTileCols);
+    unsigned int strip_done = 0;   // tiles of this strip counted before this one
+    if constexpr (OP == kChannelCast) {
+      // This tile's copy of the strip's maxima has landed: count it now and
+      // look at the result after the cast (the atomic's latency overlaps it).
+      if (ok && gw == 0 && lane == 0) strip_done = atomicAdd(&p.strip_count[cb], 1u);
+      // 128 column scales for this tile, one thread per column, before the
+      // tile's data is read (the stage is released after the reads below)
+      const int c = gw * 32 + lane;
+      if (ok && c < kTileCols) {
+        const float amax = __uint_as_float(
+            reinterpret_cast<const unsigned int*>(smem + (stage - base) + kTileBytes)[c]);
+        const GroupScale g = group_scale<FMT, POW2>(amax);
+        buf[c] = g.s;
+        buf[kTileCols + c] = g.inv;
+        const int k = cb * kTileCols + c;
+        if (rb == 0 && k < p.K) {            // each channel's scale written once
+          if (p.ue8m0)
+            p.scales[k] = (uint8_t)g.e;
+          else
+            reinterpret_cast<float*>(p.scales)[k] = g.s;
+        }
+      }
+      if (group_any(1 + group, !ok)) break;
+    }
     uint4 v[kSteps];
     if (ok) {
-      const uint32_t src = base + (uint32_t)(s * kTileBytes) +
+      const uint32_t src = stage +
                            (uint32_t)((gw * kWarpRows + half) * kRowBytes + chunk * 16);
 #pragma unroll
       for (int j = 0; j < kSteps; ++j) v[j] = lds16(src + (uint32_t)(2 * j * kRowBytes));
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);   // data now in registers
     }
-    float* buf = red + (n & 1) * (kGroupWarps * kTileCols);
 
     if constexpr (OP == kBlockCast) {
       float m = 0.0f;
@@ -348,11 +406,10 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
         if (k < p.K && m > 0.0f) atomicMax(&p.col_amax[k], __float_as_uint(m));
       }
     } else {   // kChannelCast
-      if (!ok) break;
       if (col < p.K) {
         float sv[8], iv[8];
-        const float4* sp = reinterpret_cast<const float4*>(p.col_s + col);
-        const float4* ip = reinterpret_cast<const float4*>(p.col_s + p.k_pad + col);
+        const float4* sp = reinterpret_cast<const float4*>(buf + chunk * 8);
+        const float4* ip = reinterpret_cast<const float4*>(buf + kTileCols + chunk * 8);
         const float4 s0 = sp[0], s1 = sp[1], i0 = ip[0], i1 = ip[1];
         sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
         sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
@@ -364,45 +421,28 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
           if (row < p.M) cast8<FMT, POW2>(code_ptr<FMT>(p, row, col), v[j], sv, iv);
         }
       }
+      // The last tile of the strip to count itself clears the strip for the
+      // next call: every tile of the strip has its copy of the maxima.
+      if (gw == 0) {
+        const unsigned int done = __shfl_sync(0xFFFFFFFFu, strip_done, 0);
+        if (done == (unsigned int)(p.n_rb - 1)) {
+          for (int c = lane; c < kTileCols; c += 32) p.col_amax[cb * kTileCols + c] = 0u;
+          if (lane == 0) p.strip_count[cb] = 0u;
+        }
+      }
     }
-  }
-}
-
-// Per-channel step 2: the scale of each channel from its column amax.
-template <int FMT, bool POW2>
-__global__ void __launch_bounds__(256) column_scale_kernel(const TileParams p) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int c = (int)blockIdx.x * 256 + (int)threadIdx.x;
-  if (c < p.K) {
-    const GroupScale g = group_scale<FMT, POW2>(__uint_as_float(p.col_amax[c]));
-    p.col_s[c] = g.s;
-    p.col_s[p.k_pad + c] = g.inv;
-    if (p.ue8m0)
-      p.scales[c] = (uint8_t)g.e;
-    else
-      reinterpret_cast<float*>(p.scales)[c] = g.s;
-  } else if (p.ue8m0 && c < ((p.K + 3) & ~3)) {
-    p.scales[c] = 0;   // unused bytes of the last packed word
   }
 }
 
 // ------------------------------------------------------------ host side
 
 using TileKernel = void (*)(CUtensorMap, TileParams);
-using ScaleKernel = void (*)(TileParams);
 
 template <int OP>
 TileKernel pick_tile(int fmt, bool pow2) {
   if (fmt == TK_FMT_E4M3)
     return pow2 ? tile_cast_kernel<TK_FMT_E4M3, true, OP> : tile_cast_kernel<TK_FMT_E4M3, false, OP>;
   return pow2 ? tile_cast_kernel<TK_FMT_E2M1, true, OP> : tile_cast_kernel<TK_FMT_E2M1, false, OP>;
-}
-
-ScaleKernel pick_scale(int fmt, bool pow2) {
-  if (fmt == TK_FMT_E4M3)
-    return pow2 ? column_scale_kernel<TK_FMT_E4M3, true> : column_scale_kernel<TK_FMT_E4M3, false>;
-  return pow2 ? column_scale_kernel<TK_FMT_E2M1, true> : column_scale_kernel<TK_FMT_E2M1, false>;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -450,7 +490,8 @@ tk_status launch_tile(TileKernel fn, const CUtensorMap& map, const TileParams& p
   int sms = 0;
   cudaError_t err = tk_internal::prepare_kernel(reinterpret_cast<const void*>(fn), kSmemBytes, &sms);
   if (err != cudaSuccess) return cuda_fail(err);
-  const int grid = p.n_tiles < sms ? p.n_tiles : sms;
+  const int slots = sms * kCtasPerSm;
+  const int grid = p.n_tiles < slots ? p.n_tiles : slots;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = dependent_launch(attr, (unsigned)grid, kThreads, kSmemBytes, stream);
   err = cudaLaunchKernelEx(&cfg, fn, map, p);
@@ -488,6 +529,7 @@ TileParams base_params(int64_t M, int64_t K, int mode, void* codes, int64_t ld_c
   p.M = (int)M;
   p.K = (int)K;
   p.n_cb = (int)((K + kTileCols - 1) / kTileCols);
+  p.n_rb = (int)((M + kTileRows - 1) / kTileRows);
   p.k_pad = p.n_cb * kTileCols;
   p.ue8m0 = mode == TK_SCALE_UE8M0_PACKED ? 1 : 0;
   return p;
@@ -514,8 +556,8 @@ extern "C" {
 
 size_t tk_per_channel_workspace_bytes(int64_t K) {
   if (K <= 0 || K > (int64_t(1) << 28)) return 0;
-  const int64_t k_pad = (K + kTileCols - 1) / kTileCols * kTileCols;
-  return (size_t)(12 * k_pad);
+  const int64_t n_cb = (K + kTileCols - 1) / kTileCols;
+  return (size_t)(4 * n_cb * kTileCols + (4 * n_cb + 15) / 16 * 16);
 }
 
 tk_status tk_per_block_cast(const void* x, int64_t M, int64_t K, int64_t ld_x, int fmt,
@@ -558,27 +600,16 @@ tk_status tk_per_channel_cast(const void* x, int64_t M, int64_t K, int64_t ld_x,
   TileParams p = base_params(M, K, mode, codes, ld_codes, scales);
   p.n_tiles = (int)n_tiles;
   p.col_amax = static_cast<unsigned int*>(workspace);
-  p.col_s = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 4 * (size_t)p.k_pad);
+  p.strip_count = p.col_amax + p.k_pad;
   CUtensorMap map;
   st = make_map(&map, x, M, K, ld_x);
   if (st != TK_OK) return st;
   const bool pow2 = mode != TK_SCALE_FP32;
 
-  // 0. column maxima start at +0 (the bit pattern 0)
-  cudaError_t err = cudaMemsetAsync(p.col_amax, 0, 4 * (size_t)p.k_pad,
-                                    static_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) return cuda_fail(err);
-  // 1. column amax
+  // 1. column amax (the maxima start at +0, the bit pattern 0)
   st = launch_tile(tile_cast_kernel<TK_FMT_E4M3, false, kColumnAmax>, map, p, stream);
   if (st != TK_OK) return st;
-  // 2. column scales
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg =
-      dependent_launch(attr, (unsigned)((p.k_pad + 255) / 256), 256, 0, stream);
-  err = cudaLaunchKernelEx(&cfg, pick_scale(fmt, pow2), p);
-  if (err == cudaSuccess) err = cudaGetLastError();
-  if (err != cudaSuccess) return cuda_fail(err);
-  // 3. cast
+  // 2. cast (column scales computed per tile from the maxima)
   return launch_tile(pick_tile<kChannelCast>(fmt, pow2), map, p, stream);
 }
 

@@ -185,7 +185,7 @@ WS = 0x40000
 
 
 def call_pc(lib, *, x=A, M=4, K=256, ld_x=256, fmt=0, mode=0, codes=B,
-            ld_codes=256, scales=C, ws=WS, ws_bytes=12 * 256):
+            ld_codes=256, scales=C, ws=WS, ws_bytes=4 * 256 + 16):
     return lib.tk_per_channel_cast(x, M, K, ld_x, fmt, mode, codes, ld_codes,
                                    scales, ws, ws_bytes, None)
 
@@ -196,9 +196,9 @@ PC_CASES = [
     ("K not multiple of 16", dict(K=120, ld_x=128), INVALID),
     ("ld_x < K", dict(ld_x=128), INVALID),
     ("ld_codes < K", dict(ld_codes=128), INVALID),
-    ("workspace too small", dict(ws_bytes=12 * 256 - 1), INVALID),
+    ("workspace too small", dict(ws_bytes=4 * 256 + 15), INVALID),
     ("workspace for padded K", dict(K=272, ld_x=272, ld_codes=272,
-                                    ws_bytes=12 * 272), INVALID),
+                                    ws_bytes=4 * 384 + 15), INVALID),
     ("null workspace", dict(ws=None), INVALID),
     ("null x", dict(x=None), INVALID),
     ("null scales", dict(scales=None), INVALID),
@@ -216,9 +216,11 @@ def test_per_channel_validation(lib, name, kw, want):
 
 
 def test_per_channel_workspace_size(lib):
-    assert tk.tk_per_channel_workspace_bytes(256) == 12 * 256
-    assert tk.tk_per_channel_workspace_bytes(16) == 12 * 128
-    assert tk.tk_per_channel_workspace_bytes(7168) == 12 * 7168
+    # maxima for K rounded up to 128 channels + one counter per 128 (16-B units)
+    assert tk.tk_per_channel_workspace_bytes(256) == 4 * 256 + 16
+    assert tk.tk_per_channel_workspace_bytes(16) == 4 * 128 + 16
+    assert tk.tk_per_channel_workspace_bytes(7168) == 4 * 7168 + 224
+    assert tk.tk_per_channel_workspace_bytes(8 * 128 + 16) == 4 * 9 * 128 + 48
     assert tk.tk_per_channel_workspace_bytes(0) == 0
     assert tk.tk_per_channel_workspace_bytes(-5) == 0
 

@@ -85,14 +85,16 @@ def run_channel(bits, fmt, mode, ld_x=None, code_pad=0, workspace=None):
 
     xd, cd, sd = _dev(x, np.int16), _dev(codes), _dev(scales, np.int32)
     need = tk.tk_per_channel_workspace_bytes(K)
-    if workspace is None:     # contents on entry must not matter: fill with junk
-        workspace = torch.full((need,), 0xEE, dtype=torch.uint8, device="cuda")
+    if workspace is None:     # zero-filled before first use
+        workspace = torch.zeros(need + 64, dtype=torch.uint8, device="cuda")[:need]
     tk.tk_per_channel_cast(xd.data_ptr(), M, K, ld_x, tk.FMT[fmt],
                            tk.SCALE[mode], cd.data_ptr() + ld_codes, ld_codes,
                            sd.data_ptr() + 16, workspace.data_ptr(),
                            workspace.numel(), _stream())
     torch.cuda.synchronize()
     gc, gs = cd.cpu().numpy(), sd.cpu().numpy().view(np.uint32)
+    # every completed call leaves the workspace zero-filled
+    assert not workspace.cpu().numpy().any(), "workspace not left zero-filled"
 
     rc, rs = codes.copy(), scales.copy()
     s_view = rs[4:4 + nw].view(np.int32 if mode == "ue8m0" else np.float32)
@@ -210,15 +212,20 @@ def test_every_bf16_value(fmt):
 
 
 def test_workspace_reused_across_calls():
-    """Two calls in a row on one workspace: the second does not see the
-    first's column maxima."""
+    """Calls in a row on one workspace, with different shapes: none sees an
+    earlier call's column maxima, and each leaves the workspace zero."""
     torch = torch_mod()
-    ws = torch.empty(tk.tk_per_channel_workspace_bytes(512), dtype=torch.uint8,
+    ws = torch.zeros(tk.tk_per_channel_workspace_bytes(4096), dtype=torch.uint8,
                      device="cuda")
     big = random_bf16(1, 200, 512, scale=100.0)
     small = random_bf16(2, 200, 512, scale=0.01)
     assert_same(*run_channel(big, "e4m3", "fp32", workspace=ws))
     assert_same(*run_channel(small, "e4m3", "fp32", workspace=ws))
+    assert_same(*run_channel(random_bf16(3, 1000, 4096), "e2m1", "ue8m0",
+                             workspace=ws))
+    assert_same(*run_channel(random_bf16(4, 7, 160, scale=1e-3), "e4m3",
+                             "pow2", workspace=ws))
+    assert_same(*run_channel(big, "e4m3", "fp32", workspace=ws))
 
 
 def test_empty_batch_is_a_noop():
