@@ -296,4 +296,82 @@ __device__ __forceinline__ float quotient(float x, const GroupScale& g) {
   return q;
 }
 
+// ------------------------------------------------------- packed pairs
+//
+// Two-wide forms of the steps above for BF16 input, using the packed fp32
+// instructions of sm_100 and later (mul/fma .rn.f32x2: each half is one
+// IEEE operation, the same as its scalar form) and the packed BF16 max.
+// They give bit-identical results to the scalar steps with half the
+// arithmetic instructions.
+
+// Two fp32 values in one 64-bit register, `lo` in the low half.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Per half, max(|a|, |b|) of two BF16 pairs (exact; the sign bits of the
+// result are the XOR of the operands' signs and carry no meaning).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// max |x| over the 8 BF16 values of a 16-byte chunk, still as a BF16 pair.
+__device__ __forceinline__ uint32_t bmax_chunk(const uint4& q) {
+  return bmax2(bmax2(q.x, q.y), bmax2(q.z, q.w));
+}
+
+// The larger magnitude of a BF16 pair from bmax2, as fp32 (exact).
+__device__ __forceinline__ float bmax_value(uint32_t m) {
+  return fmaxf(__uint_as_float((m << 16) & 0x7FFFFFFFu), __uint_as_float(m & 0x7FFF0000u));
+}
+
+// Quotients of the two BF16 values in `w` (element 0 in the low half).
+// Power-of-two scales: the exact products x * 2^-k, with inv2 = (2^-k, 2^-k)
+// or any per-half pair of such powers.  fp32 scales: quotient()'s sequence
+// written on negated operands, with s2 the scales and ninv2 the negated
+// reciprocals RN(1/s) of the two halves:
+//   q0 = RN((-x) * (-inv))        = RN(x * inv), same sign: quotient's q0
+//   r  = RN(q0 * s + (-x))        = quotient's residual before its negation
+//   q  = RN(r * (-inv) + q0)      = quotient's RN((-r) * inv + q0)
+// Each line has the same exact operand value and the same sign for every
+// zero term as quotient()'s, so q is bit-identical (signed zeros included);
+// -x is the BF16 pair with both sign bits flipped, widened.
+template <bool POW2>
+__device__ __forceinline__ void quotient2(uint32_t w, uint64_t s2, uint64_t inv2,
+                                          float& q_lo, float& q_hi) {
+  if constexpr (POW2) {
+    asm("{\n\t.reg .b32 lo, hi;\n\t.reg .b64 x, q;\n\t"
+        "shl.b32 lo, %2, 16;\n\t"
+        "and.b32 hi, %2, 0xFFFF0000;\n\t"
+        "mov.b64 x, {lo, hi};\n\t"
+        "mul.rn.f32x2 q, x, %3;\n\t"
+        "mov.b64 {%0, %1}, q;\n\t}"
+        : "=f"(q_lo), "=f"(q_hi)
+        : "r"(w), "l"(inv2));
+  } else {
+    asm("{\n\t.reg .b32 n, lo, hi;\n\t.reg .b64 nx, q0, r, q;\n\t"
+        "xor.b32 n, %2, 0x80008000;\n\t"
+        "shl.b32 lo, n, 16;\n\t"
+        "and.b32 hi, n, 0xFFFF0000;\n\t"
+        "mov.b64 nx, {lo, hi};\n\t"
+        "mul.rn.f32x2 q0, nx, %4;\n\t"
+        "fma.rn.f32x2 r, q0, %3, nx;\n\t"
+        "fma.rn.f32x2 q, r, %4, q0;\n\t"
+        "mov.b64 {%0, %1}, q;\n\t}"
+        : "=f"(q_lo), "=f"(q_hi)
+        : "r"(w), "l"(s2), "l"(inv2));
+  }
+}
+
+// quotient2's reciprocal operand for a scale: 2^-k for power-of-two
+// scales, the negated reciprocal for fp32 scales.
+template <bool POW2>
+__device__ __forceinline__ float quotient2_inv(const GroupScale& g) {
+  return POW2 ? g.inv : -g.inv;
+}
+
 }  // namespace

@@ -168,26 +168,18 @@ __device__ __forceinline__ bool group_any(int id, bool pred) {
   return r != 0;
 }
 
-__device__ __forceinline__ float bf16_lane(const uint4& q, int e) {
-  const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
-  return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
-}
-
 // Eight channels (one 16-byte chunk of a tile row) -> codes at dst: 8 bytes
-// (E4M3) or 4 bytes (E2M1, element 0 in the low nibble), channel e divided
-// by (s[e], inv[e]).
+// (E4M3) or 4 bytes (E2M1, element 0 in the low nibble).  Channels 2k and
+// 2k+1 are divided with the scale pair s2[k] and reciprocal pair i2[k]
+// (quotient2 operands).
 template <int FMT, bool POW2>
 __device__ __forceinline__ void cast8(uint8_t* dst, const uint4& raw,
-                                      const float (&s)[8], const float (&inv)[8]) {
+                                      const uint64_t (&s2)[4], const uint64_t (&i2)[4]) {
   float q[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    GroupScale g;
-    g.s = s[e];
-    g.inv = inv[e];
-    g.e = 0;
-    q[e] = quotient<POW2>(bf16_lane(raw, e), g);
-  }
+  quotient2<POW2>(raw.x, s2[0], i2[0], q[0], q[1]);
+  quotient2<POW2>(raw.y, s2[1], i2[1], q[2], q[3]);
+  quotient2<POW2>(raw.z, s2[2], i2[2], q[4], q[5]);
+  quotient2<POW2>(raw.w, s2[3], i2[3], q[6], q[7]);
   if constexpr (FMT == TK_FMT_E4M3) {
     *reinterpret_cast<uint2*>(dst) =
         make_uint2(cvt_e4m3x4(q[0], q[1], q[2], q[3]), cvt_e4m3x4(q[4], q[5], q[6], q[7]));
@@ -319,7 +311,7 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
             reinterpret_cast<const unsigned int*>(smem + (stage - base) + kTileBytes)[c]);
         const GroupScale g = group_scale<FMT, POW2>(amax);
         buf[c] = g.s;
-        buf[kTileCols + c] = g.inv;
+        buf[kTileCols + c] = quotient2_inv<POW2>(g);
         const int k = cb * kTileCols + c;
         if (rb == 0 && k < p.K) {            // each channel's scale written once
           if (p.ue8m0)
@@ -343,10 +335,10 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
     if constexpr (OP == kBlockCast) {
       float m = 0.0f;
       if (ok) {
+        uint32_t mm = bmax_chunk(v[0]);
 #pragma unroll
-        for (int j = 0; j < kSteps; ++j)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(bf16_lane(v[j], e)));
+        for (int j = 1; j < kSteps; ++j) mm = bmax2(mm, bmax_chunk(v[j]));
+        m = bmax_value(mm);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
         if (lane == 0) buf[gw] = m;
@@ -356,11 +348,12 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
 #pragma unroll
       for (int w = 1; w < kGroupWarps; ++w) bmax = fmaxf(bmax, buf[w]);
       const GroupScale g = group_scale<FMT, POW2>(bmax);
-      float sv[8], iv[8];
+      const float gi = quotient2_inv<POW2>(g);
+      uint64_t sv[4], iv[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        sv[e] = g.s;
-        iv[e] = g.inv;
+      for (int k = 0; k < 4; ++k) {
+        sv[k] = pack_f32x2(g.s, g.s);
+        iv[k] = pack_f32x2(gi, gi);
       }
       if (col < p.K) {
 #pragma unroll
@@ -381,15 +374,23 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
       }
     } else if constexpr (OP == kColumnAmax) {
       if (ok) {
+        // per channel pair, the largest magnitude over this lane's rows and
+        // then over the other half-warp's rows (same channels)
+        uint32_t cw[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+#pragma unroll
+        for (int j = 1; j < kSteps; ++j) {
+          cw[0] = bmax2(cw[0], v[j].x);
+          cw[1] = bmax2(cw[1], v[j].y);
+          cw[2] = bmax2(cw[2], v[j].z);
+          cw[3] = bmax2(cw[3], v[j].w);
+        }
         float cm[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) cm[e] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kSteps; ++j)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) cm[e] = fmaxf(cm[e], fabsf(bf16_lane(v[j], e)));
-#pragma unroll
-        for (int e = 0; e < 8; ++e) cm[e] = fmaxf(cm[e], __shfl_xor_sync(0xFFFFFFFFu, cm[e], 16));
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t o = bmax2(cw[k], __shfl_xor_sync(0xFFFFFFFFu, cw[k], 16));
+          cm[2 * k] = __uint_as_float((o << 16) & 0x7FFFFFFFu);
+          cm[2 * k + 1] = __uint_as_float(o & 0x7FFF0000u);
+        }
         if (half == 0) {
           float4* d = reinterpret_cast<float4*>(buf + gw * kTileCols + chunk * 8);
           d[0] = make_float4(cm[0], cm[1], cm[2], cm[3]);
@@ -407,14 +408,13 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
       }
     } else {   // kChannelCast
       if (col < p.K) {
-        float sv[8], iv[8];
         const float4* sp = reinterpret_cast<const float4*>(buf + chunk * 8);
         const float4* ip = reinterpret_cast<const float4*>(buf + kTileCols + chunk * 8);
         const float4 s0 = sp[0], s1 = sp[1], i0 = ip[0], i1 = ip[1];
-        sv[0] = s0.x; sv[1] = s0.y; sv[2] = s0.z; sv[3] = s0.w;
-        sv[4] = s1.x; sv[5] = s1.y; sv[6] = s1.z; sv[7] = s1.w;
-        iv[0] = i0.x; iv[1] = i0.y; iv[2] = i0.z; iv[3] = i0.w;
-        iv[4] = i1.x; iv[5] = i1.y; iv[6] = i1.z; iv[7] = i1.w;
+        const uint64_t sv[4] = {pack_f32x2(s0.x, s0.y), pack_f32x2(s0.z, s0.w),
+                                pack_f32x2(s1.x, s1.y), pack_f32x2(s1.z, s1.w)};
+        const uint64_t iv[4] = {pack_f32x2(i0.x, i0.y), pack_f32x2(i0.z, i0.w),
+                                pack_f32x2(i1.x, i1.y), pack_f32x2(i1.z, i1.w)};
 #pragma unroll
         for (int j = 0; j < kSteps; ++j) {
           const int row = r0 + 2 * j;

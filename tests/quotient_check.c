@@ -11,10 +11,16 @@
  *     quotients carry x's sign and lie below half the format's smallest step
  *     (2^-10 for E4M3, 0.25 for E2M1), so both encode to the same signed
  *     zero -- the code, which is all the cast keeps, is identical.
+ * It also evaluates the packed kernels' form of the same sequence, written
+ * on negated operands (nx = -x, ninv = -inv):
+ *          q0' = RN(nx*ninv);  r' = RN(q0'*s + nx) (fused);
+ *          q' = RN(r'*ninv + q0') (fused)
+ * and counts the pairs where q' and q differ in any bit (there must be none).
  * Test infrastructure; compiled by tests/test_quotient_proof.py.
  * Usage: quotient_check <fmt_max>
- * Prints "pairs bad tiny tiny_bad": bad = mismatches with |RN(x/s)| >= 2^-64,
- * tiny = mismatches below it, tiny_bad = those that would change the code.
+ * Prints "pairs bad tiny tiny_bad form_diff": bad = mismatches with
+ * |RN(x/s)| >= 2^-64, tiny = mismatches below it, tiny_bad = those that
+ * would change the code, form_diff = pairs where the two forms differ.
  */
 #include <math.h>
 #include <stdint.h>
@@ -40,7 +46,7 @@ static uint32_t bits(float f)
 int main(int argc, char **argv)
 {
     float fmt_max = argc > 1 ? (float)atof(argv[1]) : 448.0f;
-    unsigned long long pairs = 0, bad = 0, sub = 0, sub_bad = 0;
+    unsigned long long pairs = 0, bad = 0, sub = 0, sub_bad = 0, form = 0;
     float half_step = fmt_max == 448.0f ? 0x1p-10f : 0.25f;
     for (uint32_t ab = 0; ab <= 0x7F7Fu; ++ab) {
         float a = bf16(ab);
@@ -56,6 +62,12 @@ int main(int argc, char **argv)
                  * into the first FMA, which would not preserve -0 */
                 volatile float r = fmaf(q0, s, -x);
                 float q = fmaf(-r, inv, q0);
+                volatile float nx = -x, ninv = -inv;
+                float q0n = nx * ninv;
+                float rn = fmaf(q0n, s, nx);
+                float qn = fmaf(rn, ninv, q0n);
+                if (bits(qn) != bits(q))
+                    form++;
                 pairs++;
                 if (bits(q) == bits(want))
                     continue;
@@ -74,6 +86,6 @@ int main(int argc, char **argv)
             }
         }
     }
-    printf("%llu %llu %llu %llu\n", pairs, bad, sub, sub_bad);
+    printf("%llu %llu %llu %llu %llu\n", pairs, bad, sub, sub_bad, form);
     return 0;
 }

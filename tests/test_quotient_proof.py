@@ -54,13 +54,31 @@ def test_kernel_uses_the_checked_sequence():
     assert '"f"(x), "f"(g.inv), "f"(g.s)' in body
 
 
+def test_packed_kernels_use_the_negated_form():
+    """quotient2 (fp32 scales): nx = -x from the sign-flipped BF16 pair;
+    q0 = nx*ninv; r = fma(q0, s, nx); q = fma(r, ninv, q0), with ninv the
+    negated reciprocal (quotient2_inv) -- the form the checker compares."""
+    src = open(CU).read()
+    body = src[src.index("__device__ __forceinline__ void quotient2("):]
+    body = body[body.index("} else {"):body.index("quotient2_inv")]
+    seq = re.findall(r'"(xor\.b32|mul\.rn\.f32x2|fma\.rn\.f32x2) ([^;]*);', body)
+    assert seq == [("xor.b32", "n, %2, 0x80008000"),
+                   ("mul.rn.f32x2", "q0, nx, %4"),
+                   ("fma.rn.f32x2", "r, q0, %3, nx"),
+                   ("fma.rn.f32x2", "q, r, %4, q0")], seq
+    assert '"r"(w), "l"(s2), "l"(inv2)' in body
+    inv = src[src.index("float quotient2_inv("):]
+    assert "return POW2 ? g.inv : -g.inv;" in inv[:200]
+
+
 @pytest.mark.parametrize("fmt_max", ["448", "6"])
 def test_every_reachable_pair(checker, fmt_max):
     out = subprocess.run([checker, fmt_max], check=True, capture_output=True,
                          text=True, timeout=600)
-    pairs, bad, sub, sub_bad = map(int, out.stdout.split())
+    pairs, bad, sub, sub_bad, form = map(int, out.stdout.split())
     assert pairs > 10 ** 9
     assert bad == 0, out.stderr
     assert sub_bad == 0
+    assert form == 0, "the negated-operand form differs from the sequence"
     print(f"{pairs} pairs; {sub} quotients below 2^-64 off by the residual "
           "underflow, all encoding to the same signed zero")
