@@ -243,6 +243,31 @@ TK_API tk_status tk_per_channel_cast(const void *x, int64_t M, int64_t K,
                                      size_t workspace_bytes, void *stream);
 
 /*
+ * tk_per_channel_cast_noalloc -- tk_per_channel_cast without a caller
+ * workspace.  The pages have no counterpart: it is an interface for
+ * callers that cannot allocate device memory where they call the cast (a
+ * C host without a caching allocator, where cudaMalloc and cudaFree
+ * synchronise the device; a serving loop that allows no allocation after
+ * warm-up).  The workspace is a fixed array in the library's static device
+ * memory, one per device.
+ *
+ *   Arguments and results as for tk_per_channel_cast, with K <= 65536
+ *   (TK_ERR_UNSUPPORTED beyond: the array holds the workspace of 65,536
+ *   channels, 264,192 bytes).
+ *   The first call on each device finds the array (cudaGetSymbolAddress)
+ *   and clears it with a synchronous cudaMemset; make that first call
+ *   outside any stream capture.
+ *   All calls on one device share the array: calls that may overlap in
+ *   time (other streams, other host threads) race on it and give wrong
+ *   results; the caller must order them (one stream, or events).
+ */
+TK_API tk_status tk_per_channel_cast_noalloc(const void *x, int64_t M,
+                                             int64_t K, int64_t ld_x,
+                                             int fmt, int mode, void *codes,
+                                             int64_t ld_codes, void *scales,
+                                             void *stream);
+
+/*
  * tk_get_device_fault -- read (and optionally clear) the library's device
  * fault words on the current device (the OR of the per-token kernels' word
  * and the per-block / per-channel kernels' word).  Every wait inside the kernels is

@@ -19,6 +19,8 @@ Low level (same names and arguments as the C ABI, raw pointers and sizes):
     tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
                         scales_ptr, workspace_ptr, workspace_bytes, stream)
     tk_per_channel_workspace_bytes(K)
+    tk_per_channel_cast_noalloc(x_ptr, M, K, ld_x, fmt, mode, codes_ptr,
+                                ld_codes, scales_ptr, stream)
 
 Tensor level (allocates outputs with torch):
     codes, scales = per_token_cast(x, group=128, fmt="e4m3", scale="fp32",
@@ -103,6 +105,9 @@ def load():
             lib.tk_per_channel_cast.argtypes = [p, i64, i64, i64, i, i, p, i64,
                                                 p, p, ctypes.c_size_t, p]
             lib.tk_per_channel_cast.restype = i
+            lib.tk_per_channel_cast_noalloc.argtypes = [p, i64, i64, i64, i, i,
+                                                        p, i64, p, p]
+            lib.tk_per_channel_cast_noalloc.restype = i
             lib.tk_per_channel_workspace_bytes.argtypes = [i64]
             lib.tk_per_channel_workspace_bytes.restype = ctypes.c_size_t
             lib.tk_get_device_fault.argtypes = [p, i]
@@ -172,6 +177,15 @@ def tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
     _check(load().tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr,
                                       ld_codes, scales_ptr, workspace_ptr,
                                       workspace_bytes, stream))
+
+
+def tk_per_channel_cast_noalloc(x_ptr, M, K, ld_x, fmt, mode, codes_ptr,
+                                ld_codes, scales_ptr, stream=0) -> None:
+    """Raw-pointer call of the per-channel cast on the library's static
+    per-device workspace (K <= 65536; calls must not overlap in time)."""
+    _check(load().tk_per_channel_cast_noalloc(x_ptr, M, K, ld_x, fmt, mode,
+                                              codes_ptr, ld_codes, scales_ptr,
+                                              stream))
 
 
 def tk_per_channel_workspace_bytes(K: int) -> int:

@@ -535,6 +535,54 @@ TileParams base_params(int64_t M, int64_t K, int mode, void* codes, int64_t ld_c
   return p;
 }
 
+// --------------------------------------------- allocation-free variant
+//
+// tk_per_channel_cast_noalloc runs tk_per_channel_cast on a workspace that
+// lives in static device memory instead of one the caller provides.  Callers
+// that cannot allocate device memory at the point of the call use it: a C
+// host without a caching allocator (cudaMalloc/cudaFree synchronise the
+// device), or a serving loop that forbids allocation after warm-up.  Its
+// limit is the size of the array below: at most kNoAllocMaxChannels
+// channels.
+
+constexpr int64_t kNoAllocMaxChannels = 65536;
+constexpr size_t kNoAllocScratchBytes =
+    (size_t)(4 * kNoAllocMaxChannels + (4 * (kNoAllocMaxChannels / TK_BLOCK) + 15) / 16 * 16);
+
+static __device__ __align__(256) unsigned char g_channel_scratch[kNoAllocScratchBytes];
+
+// Per device: the scratch's address, found and cleared once.
+struct ScratchTable {
+  std::mutex mu;
+  static constexpr int kMaxDev = 64;
+  void* addr[kMaxDev] = {};
+};
+ScratchTable g_scratch;
+
+// The current device's scratch: on the first call for a device, its address
+// (cudaGetSymbolAddress) and one clearing memset, since the per-channel
+// workspace must be zero-filled before its first use.  That memset is
+// synchronous, so the first call on each device must not be made while a
+// stream is being captured.
+tk_status channel_scratch(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (dev < 0 || dev >= ScratchTable::kMaxDev) return TK_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch.mu);
+  if (g_scratch.addr[dev] == nullptr) {
+    void* addr = nullptr;
+    err = cudaGetSymbolAddress(&addr, g_channel_scratch);
+    if (err != cudaSuccess) return cuda_fail(err);
+    if (addr == nullptr || !aligned(addr, 256)) return TK_ERR_CUDA;
+    err = cudaMemset(addr, 0, kNoAllocScratchBytes);
+    if (err != cudaSuccess) return cuda_fail(err);
+    g_scratch.addr[dev] = addr;
+  }
+  *out = g_scratch.addr[dev];
+  return TK_OK;
+}
+
 }  // namespace
 
 namespace tk_internal {
@@ -611,6 +659,23 @@ tk_status tk_per_channel_cast(const void* x, int64_t M, int64_t K, int64_t ld_x,
   if (st != TK_OK) return st;
   // 2. cast (column scales computed per tile from the maxima)
   return launch_tile(pick_tile<kChannelCast>(fmt, pow2), map, p, stream);
+}
+
+tk_status tk_per_channel_cast_noalloc(const void* x, int64_t M, int64_t K, int64_t ld_x,
+                                      int fmt, int mode, void* codes, int64_t ld_codes,
+                                      void* scales, void* stream) {
+  tk_status st = check_tile_args(M, K, ld_x, fmt, mode, ld_codes);
+  if (st != TK_OK) return st;
+  if (K > kNoAllocMaxChannels) return TK_ERR_UNSUPPORTED;
+  if (tk_per_channel_workspace_bytes(K) > kNoAllocScratchBytes) return TK_ERR_UNSUPPORTED;
+  if (M == 0) return TK_OK;
+  st = check_tile_pointers(x, ld_x, codes, ld_codes, scales);
+  if (st != TK_OK) return st;
+  void* scratch = nullptr;
+  st = channel_scratch(&scratch);
+  if (st != TK_OK) return st;
+  return tk_per_channel_cast(x, M, K, ld_x, fmt, mode, codes, ld_codes, scales, scratch,
+                             kNoAllocScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -215,6 +215,33 @@ def test_per_channel_validation(lib, name, kw, want):
     assert call_pc(lib, **kw) == want
 
 
+def call_na(lib, *, x=A, M=4, K=256, ld_x=256, fmt=0, mode=0, codes=B,
+            ld_codes=256, scales=C):
+    return lib.tk_per_channel_cast_noalloc(x, M, K, ld_x, fmt, mode, codes,
+                                           ld_codes, scales, None)
+
+
+NA_CASES = [
+    ("bad fmt", dict(fmt=2), INVALID),
+    ("bad mode", dict(mode=3), INVALID),
+    ("K not multiple of 16", dict(K=200, ld_x=256), INVALID),
+    ("ld_codes < K", dict(ld_codes=128), INVALID),
+    ("null x", dict(x=None), INVALID),
+    ("x misaligned", dict(x=A + 8), MISALIGNED),
+    ("scales misaligned", dict(scales=C + 2), MISALIGNED),
+    ("beyond the static workspace", dict(K=65536 + 16, ld_x=65536 + 16,
+                                         ld_codes=65536 + 16), UNSUPPORTED),
+    ("beyond it even with M = 0", dict(M=0, K=65536 + 16, ld_x=65536 + 16,
+                                       ld_codes=65536 + 16), UNSUPPORTED),
+    ("empty batch", dict(M=0, x=None, codes=None, scales=None), OK),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", NA_CASES, ids=[c[0] for c in NA_CASES])
+def test_per_channel_noalloc_validation(lib, name, kw, want):
+    assert call_na(lib, **kw) == want
+
+
 def test_per_channel_workspace_size(lib):
     # maxima for K rounded up to 128 channels + one counter per 128 (16-B units)
     assert tk.tk_per_channel_workspace_bytes(256) == 4 * 256 + 16
