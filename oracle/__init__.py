@@ -78,6 +78,13 @@ def _configure(lib):
     lib.oracle_per_token_cast_back.argtypes = [p, i64, i64, i64, i64, i, i, i,
                                                p, i64]
     lib.oracle_per_token_cast_back.restype = i
+    lib.oracle_rmsnorm_values.argtypes = [p, p, i64, i64, i64, i64,
+                                          ctypes.c_float, p, i64]
+    lib.oracle_rmsnorm_values.restype = None
+    lib.oracle_rmsnorm_per_token_cast.argtypes = [p, p, i64, i64, i64, i64,
+                                                  ctypes.c_float, i, i, i, i,
+                                                  p, i64, p, i64]
+    lib.oracle_rmsnorm_per_token_cast.restype = i
     lib.oracle_per_block_cast.argtypes = [p, i64, i64, i64, i, i64, i64, i, i,
                                           p, i64, p, i64]
     lib.oracle_per_block_cast.restype = i
@@ -275,6 +282,52 @@ def per_token_cast_back(x_bits: np.ndarray, K: int, group: int, fmt: int,
 
     _split(M, threads, work)
     return y
+
+
+def rmsnorm_values(x_bits: np.ndarray, w_bits: np.ndarray, K: int,
+                   eps: float, threads: int = 1) -> np.ndarray:
+    """RMSNorm outputs y (fp32 [M, K]) of BF16 rows x with gain w."""
+    lib = _load()
+    M = x_bits.shape[0]
+    ld_x = x_bits.strides[0] // 2
+    w_bits = np.ascontiguousarray(w_bits, np.uint16)
+    y = np.empty((M, K), np.float32)
+
+    def work(a, b):
+        lib.oracle_rmsnorm_values(_ptr(x_bits), _ptr(w_bits), a, b, K, ld_x,
+                                  eps, _ptr(y), K)
+        return 0
+
+    _split(M, threads, work)
+    return y
+
+
+def rmsnorm_per_token_cast(x_bits: np.ndarray, w_bits: np.ndarray, K: int,
+                           eps: float, group: int, fmt: int, mode: int,
+                           layout: int, *, codes: np.ndarray | None = None,
+                           scales: np.ndarray | None = None,
+                           threads: int = 1):
+    """Oracle RMSNorm (gain w, eps) fused with the per-token cast of its
+    fp32 output.  Shapes as for ``per_token_cast``."""
+    lib = _load()
+    M = x_bits.shape[0]
+    ld_x = x_bits.strides[0] // 2
+    w_bits = np.ascontiguousarray(w_bits, np.uint16)
+    if codes is None:
+        codes = np.zeros((M, K if fmt == FMT_E4M3 else K // 2), np.uint8)
+    if scales is None:
+        r, c, dt = scale_shape(M, K, group, mode, layout)
+        scales = np.zeros((r, c), dt)
+    ld_codes = codes.strides[0]
+    ld_scales = scales.strides[0] // scales.itemsize
+
+    def work(a, b):
+        return lib.oracle_rmsnorm_per_token_cast(
+            _ptr(x_bits), _ptr(w_bits), a, b, K, ld_x, eps, group, fmt, mode,
+            layout, _ptr(codes), ld_codes, _ptr(scales), ld_scales)
+
+    _split(M, threads, work)
+    return codes, scales
 
 
 def block_scale_shape(M: int, K: int, block: int, mode: int):

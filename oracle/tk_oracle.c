@@ -497,6 +497,64 @@ int oracle_per_token_cast_back(const uint16_t *x, int64_t m_begin,
     return rc;
 }
 
+/* ------------------------------------------------- RMSNorm + per-token cast */
+
+/*
+ * aiwiki "TileKernels", section "Version 2.0.0": the library added RMSNorm
+ * forward and backward "with an optional fused FP8 cast".  The pages do not
+ * define RMSNorm; this follows its published definition (Zhang and Sennrich,
+ * "Root Mean Square Layer Normalization", 2019), with a learned gain w per
+ * channel and eps added to the mean square:
+ *   y_k = w_k * x_k / sqrt(eps + (1/K) * sum_j x_j^2)
+ * Formed in double (every BF16 square and product is exact there and the
+ * sum of K <= 2^28 positive terms is within a few double ulps) and rounded
+ * once to fp32; the fused cast then casts y exactly as cast_row casts an
+ * fp32 row (no BF16 intermediate).  A row of zeros with eps = 0 has no
+ * value (0/0): the cast returns OR_NONFINITE for it.
+ */
+void oracle_rmsnorm_values(const uint16_t *x, const uint16_t *w,
+                           int64_t m_begin, int64_t m_end, int64_t K,
+                           int64_t ld_x, float eps, float *y, int64_t ld_y)
+{
+    for (int64_t m = m_begin; m < m_end; ++m) {
+        const uint16_t *xr = x + m * ld_x;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)bf16_bits_to_float(xr[k]);
+            ss += v * v;
+        }
+        double rstd = 1.0 / sqrt((double)eps + ss / (double)K);
+        for (int64_t k = 0; k < K; ++k)
+            y[m * ld_y + k] = (float)((double)bf16_bits_to_float(w[k]) *
+                                      (double)bf16_bits_to_float(xr[k]) *
+                                      rstd);
+    }
+}
+
+int oracle_rmsnorm_per_token_cast(const uint16_t *x, const uint16_t *w,
+                                  int64_t m_begin, int64_t m_end, int64_t K,
+                                  int64_t ld_x, float eps, int group, int fmt,
+                                  int mode, int layout, uint8_t *codes,
+                                  int64_t ld_codes, void *scales,
+                                  int64_t ld_scales)
+{
+    int rc = check_common(K, group, fmt, mode, layout);
+    if (rc != OR_OK)
+        return rc;
+    if (!(eps >= 0.0f) || !isfinite(eps))
+        return OR_BAD_ARG;
+    float *row = (float *)malloc((size_t)K * sizeof(float));
+    if (!row)
+        return OR_BAD_ARG;
+    for (int64_t m = m_begin; m < m_end && rc == OR_OK; ++m) {
+        oracle_rmsnorm_values(x + m * ld_x, w, 0, 1, K, ld_x, eps, row, K);
+        rc = cast_row(row, K, group, fmt, mode, layout, m,
+                      codes + m * ld_codes, scales, ld_scales);
+    }
+    free(row);
+    return rc;
+}
+
 /* ------------------------------------------ per-block and per-channel cast */
 
 /*

@@ -17,6 +17,7 @@ import test_oracle_dequant as td
 import test_oracle_scale as ts
 import test_oracle_swiglu as tw
 import test_oracle_tile_cast as tt
+import test_oracle_rmsnorm as trn
 
 MUTATIONS = {
     "ties_away_e4m3": ("(dropped == 0x80000u && (keep & 1u))",
@@ -56,6 +57,21 @@ MUTATIONS = {
     "dequant_nibble_order": ("(k & 1) ? byte >> 4 : byte & 0xF", "(k & 1) ? byte & 0xF : byte >> 4"),
     "dequant_scale_transposed_index": ("                                         : base[j * ld_scales + m];",
                                        "                                         : base[m * 0 + j * ld_scales];"),
+}
+
+# Mistakes in the RMSNorm code, run against its pins.
+RMS_MUTATIONS = {
+    "rms_eps_dropped": ("double rstd = 1.0 / sqrt((double)eps + ss / (double)K);",
+                        "double rstd = 1.0 / sqrt(ss / (double)K);"),
+    "rms_sum_not_mean": ("double rstd = 1.0 / sqrt((double)eps + ss / (double)K);",
+                         "double rstd = 1.0 / sqrt((double)eps + ss);"),
+    "rms_no_root": ("double rstd = 1.0 / sqrt((double)eps + ss / (double)K);",
+                    "double rstd = 1.0 / ((double)eps + ss / (double)K);"),
+    "rms_mean_over_k_minus_1": ("ss / (double)K);", "ss / (double)(K - 1));"),
+    "rms_gain_ignored": ("y[m * ld_y + k] = (float)((double)bf16_bits_to_float(w[k]) *",
+                         "y[m * ld_y + k] = (float)((double)1.0f *"),
+    "rms_abs_not_square": ("ss += v * v;", "ss += fabs(v);"),
+    "rms_gain_of_first_channel": ("(double)bf16_bits_to_float(w[k]) *", "(double)bf16_bits_to_float(w[0]) *"),
 }
 
 # Mistakes in the per-block / per-channel code, run against those pins.
@@ -140,6 +156,27 @@ def test_planted_tile_mistake_is_caught(name, tmp_path):
     failed = []
     try:
         for fn in _pin_functions((tt,)):
+            try:
+                _call_all_params(fn)
+            except Exception:  # any failing pin counts
+                failed.append(fn.__name__)
+    finally:
+        oracle._lib = real
+    assert failed, f"no pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", sorted(RMS_MUTATIONS))
+def test_planted_rmsnorm_mistake_is_caught(name, tmp_path):
+    old, new = RMS_MUTATIONS[name]
+    src = oracle.source_text()
+    assert old in src, f"mutation anchor not found: {old!r}"
+    lib = oracle.compile_variant(src.replace(old, new, 1),
+                                 str(tmp_path / f"lib_{name}.so"))
+    real = oracle._load()
+    oracle._lib = lib
+    failed = []
+    try:
+        for fn in _pin_functions((trn,)):
             try:
                 _call_all_params(fn)
             except Exception:  # any failing pin counts
