@@ -39,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from precision_quantization_token_gb300.inputs import (WORKLOADS,  # noqa: E402
-                                                       make_input)
+                                                       make_gain, make_input)
 
 METRIC = "per-token cast GB/s (in+out bytes) and % of GB300 HBM peak at 4096x7168"
 UNIT = "GB/s"
@@ -237,6 +237,10 @@ class GpuWorkload:
                                          dtype=torch.uint8, device=device)
         else:
             shape, dt = tk.scale_shape(w.M, w.K, w.group, w.scale, w.layout)
+        if w.op == "rmsnorm":
+            g = make_gain(w)
+            self.gain = torch.from_numpy(g.view(np.int16)).view(
+                torch.bfloat16).to(device)
         if w.op == "dequant":
             # the codes and scales to dequantize come from one (untimed) cast
             c0, s0 = tk.per_token_cast(x0, w.group, w.fmt, w.scale, w.layout)
@@ -276,6 +280,14 @@ class GpuWorkload:
                                       w.group, tk.FMT[w.fmt],
                                       tk.SCALE[w.scale], b.data_ptr(),
                                       b.stride(0), stream_handle)
+        elif w.op == "rmsnorm":
+            tk.tk_rmsnorm_per_token_cast(a.data_ptr(), self.gain.data_ptr(),
+                                         w.M, w.K, a.stride(0), w.eps,
+                                         w.group, tk.FMT[w.fmt],
+                                         tk.SCALE[w.scale],
+                                         tk.LAYOUT[w.layout], b.data_ptr(),
+                                         b.stride(0), c.data_ptr(),
+                                         c.stride(0), stream_handle)
         elif w.op == "block":
             tk.tk_per_block_cast(a.data_ptr(), w.M, w.K, a.stride(0),
                                  tk.FMT[w.fmt], tk.SCALE[w.scale],

@@ -179,6 +179,35 @@ TK_API tk_status tk_per_token_cast_back(const void *x, int64_t M, int64_t K,
                                         int mode, void *y, int64_t ld_y,
                                         void *stream);
 
+/*
+ * tk_rmsnorm_per_token_cast -- RMSNorm with a fused per-token cast (aiwiki
+ * "TileKernels", section "Version 2.0.0": "RMSNorm forward ... with an
+ * optional fused FP8 cast").  RMSNorm by its published definition (Zhang
+ * and Sennrich, "Root Mean Square Layer Normalization", 2019):
+ *   y[m, k] = w[k] * x[m, k] / sqrt(eps + (1/K) * sum_j x[m, j]^2)
+ * then y is cast exactly as tk_per_token_cast casts a row (no BF16
+ * intermediate).  The kernel works in IEEE fp32: the sum of squares by
+ * fused multiply-adds in a fixed order, rstd = 1 / sqrt(sum / K + eps)
+ * with each step one correctly rounded operation, and y = RN((x * w) *
+ * rstd), where x * w is exact.  Against y formed exactly, y is within about
+ * (log2(K) + 8) fp32 ulps, so scales can differ from an exact evaluation by
+ * that many ulps (fp32 mode; power-of-two scales only near a power of two)
+ * and a small fraction of codes by one step.
+ *
+ *   x         BF16 [M][ld_x], K values per row; K <= 8192 (one row per
+ *             pipeline stage; TK_ERR_UNSUPPORTED beyond).
+ *   w         BF16 [K], the per-channel gain; 16-byte aligned.
+ *   eps       finite and >= 0 (TK_ERR_INVALID_ARG otherwise); a row of
+ *             zeros needs eps > 0 (0/0 otherwise: unspecified codes).
+ *   Other arguments as for tk_per_token_cast; y must be finite.
+ */
+TK_API tk_status tk_rmsnorm_per_token_cast(const void *x, const void *w,
+                                           int64_t M, int64_t K, int64_t ld_x,
+                                           float eps, int group, int fmt,
+                                           int mode, int layout, void *codes,
+                                           int64_t ld_codes, void *scales,
+                                           int64_t ld_scales, void *stream);
+
 /* Block edge of tk_per_block_cast (square blocks of rows x channels), and
  * the channel granularity of tk_per_channel_cast's workspace. */
 #define TK_BLOCK 128

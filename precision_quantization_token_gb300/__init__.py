@@ -14,6 +14,9 @@ Low level (same names and arguments as the C ABI, raw pointers and sizes):
                          group, fmt, mode, layout, y_ptr, ld_y, out_dtype, stream)
     tk_per_token_cast_back(x_ptr, M, K, ld_x, group, fmt, mode, y_ptr, ld_y,
                            stream)
+    tk_rmsnorm_per_token_cast(x_ptr, w_ptr, M, K, ld_x, eps, group, fmt,
+                              mode, layout, codes_ptr, ld_codes, scales_ptr,
+                              ld_scales, stream)
     tk_per_block_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
                       scales_ptr, ld_scales, stream)
     tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
@@ -28,6 +31,7 @@ Tensor level (allocates outputs with torch):
     codes, scales = swiglu_per_token_cast(x, group=128, ...)  # x = [gate|up]
     y = per_token_dequant(codes, scales, K, group=128, fmt="e4m3", ...)
     y = per_token_cast_back(x, group=128, fmt="e4m3", scale="fp32")
+    codes, scales = rmsnorm_per_token_cast(x, w, eps=1e-6, group=128, ...)
     codes, scales = per_block_cast(x, fmt="e4m3", scale="fp32")   # 128x128
     codes, scales = per_channel_cast(x, fmt="e4m3", scale="fp32")
 
@@ -99,6 +103,10 @@ def load():
             lib.tk_per_token_dequant.argtypes = [p, i64, p, i64, i64, i64, i, i,
                                                  i, i, p, i64, i, p]
             lib.tk_per_token_dequant.restype = i
+            lib.tk_rmsnorm_per_token_cast.argtypes = [p, p, i64, i64, i64,
+                                                      ctypes.c_float, i, i, i,
+                                                      i, p, i64, p, i64, p]
+            lib.tk_rmsnorm_per_token_cast.restype = i
             lib.tk_per_block_cast.argtypes = [p, i64, i64, i64, i, i, p, i64,
                                               p, i64, p]
             lib.tk_per_block_cast.restype = i
@@ -161,6 +169,17 @@ def tk_per_token_dequant(codes_ptr, ld_codes, scales_ptr, ld_scales, M, K,
     _check(load().tk_per_token_dequant(codes_ptr, ld_codes, scales_ptr,
                                        ld_scales, M, K, group, fmt, mode,
                                        layout, y_ptr, ld_y, out_dtype, stream))
+
+
+def tk_rmsnorm_per_token_cast(x_ptr, w_ptr, M, K, ld_x, eps, group, fmt,
+                              mode, layout, codes_ptr, ld_codes, scales_ptr,
+                              ld_scales, stream=0) -> None:
+    """Raw-pointer call of RMSNorm (gain w, eps) fused with the per-token
+    cast of its output."""
+    _check(load().tk_rmsnorm_per_token_cast(x_ptr, w_ptr, M, K, ld_x, eps,
+                                            group, fmt, mode, layout,
+                                            codes_ptr, ld_codes, scales_ptr,
+                                            ld_scales, stream))
 
 
 def tk_per_block_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
@@ -290,6 +309,30 @@ def swiglu_per_token_cast(x, group: int = 128, fmt: str = "e4m3",
     N = x.shape[1] // 2
     return _call(tk_swiglu_per_token_cast, x, N, group, fmt, scale, layout,
                  codes, scales, stream)
+
+
+def rmsnorm_per_token_cast(x, w, eps: float = 1e-6, group: int = 128,
+                           fmt: str = "e4m3", scale: str = "fp32",
+                           layout: str = "row", *, codes=None, scales=None,
+                           stream=None):
+    """RMSNorm of the rows of a bfloat16 [M, K] CUDA tensor with gain w
+    (bfloat16 [K]) fused with the per-token cast of the fp32 result.
+    Returns (codes, scales) as per_token_cast does."""
+    import torch
+    _check_x(x)
+    if w.dtype != torch.bfloat16 or w.dim() != 1 or w.stride(0) != 1:
+        raise ValueError("w must be a contiguous 1-D bfloat16 tensor")
+    M, K = x.shape
+    codes, scales = _outputs(torch, M, K, group, fmt, scale, layout, x.device,
+                             codes, scales)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    tk_rmsnorm_per_token_cast(x.data_ptr(), w.data_ptr(), M, K, x.stride(0),
+                              eps, group, FMT[fmt], SCALE[scale],
+                              LAYOUT[layout], codes.data_ptr(),
+                              codes.stride(0), scales.data_ptr(),
+                              scales.stride(0), stream)
+    return codes, scales
 
 
 def per_token_dequant(codes, scales, K: int, group: int = 128,

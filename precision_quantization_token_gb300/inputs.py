@@ -20,6 +20,8 @@ Workloads are the shapes and value mixes the per-token cast is measured on:
   d2   dequantization of c2's codes and scales to BF16 (4096 x 7168)
   b2   cast-and-cast-back of c2's input (4096 x 7168, E4M3 g128 UE8M0)
   pb2  per-block cast (128 x 128 blocks) of c2's input, E4M3, fp32 scales
+  r2   RMSNorm (eps 1e-6, gain 1 + 0.1 N(0,1)) fused with the per-token cast
+       of c2's input: E4M3, group 128, UE8M0 packed
   pc2  per-channel cast (one scale per column) of c2's input, E4M3, fp32
 
 Random draws use numpy's PCG64 generator seeded per workload; fp32 values are
@@ -47,7 +49,8 @@ class Workload:
     seed: int
     dist: str
     op: str = "cast"   # "cast" | "swiglu" | "dequant" | "cast_back"
-    #                  | "block" | "channel"
+    #                  | "block" | "channel" | "rmsnorm"
+    eps: float = 1e-6  # RMSNorm
 
     @property
     def in_cols(self) -> int:
@@ -83,6 +86,8 @@ class Workload:
             return {"read": read, "codes": codes, "scales": scales,
                     "total": read + codes + scales}
         read = self.M * self.in_cols * 2
+        if self.op == "rmsnorm":
+            read += self.K * 2                      # the gain vector
         return {"read": read, "codes": codes, "scales": scales,
                 "total": read + codes + scales}
 
@@ -95,7 +100,8 @@ class Workload:
                     f"{self.M}x{self.K} ({self.dist})")
         op = {"cast": "per_token_cast", "swiglu": "swiglu_per_token_cast",
               "dequant": "per_token_dequant",
-              "cast_back": "per_token_cast_back"}[self.op]
+              "cast_back": "per_token_cast_back",
+              "rmsnorm": f"rmsnorm(eps {self.eps:g})+per_token_cast"}[self.op]
         shape = (f"{self.M}x{self.in_cols}->{self.M}x{self.K}" if self.swiglu
                  else f"{self.M}x{self.K}")
         return (f"{op} {self.fmt.upper()} g{self.group} {self.scale} "
@@ -119,6 +125,8 @@ WORKLOADS = {
                    "normal, 0.1% x100 outliers", op="dequant"),
     "b2": Workload("b2", 4096, 7168, 128, "e4m3", "ue8m0", "row", False, 2,
                    "normal, 0.1% x100 outliers", op="cast_back"),
+    "r2": Workload("r2", 4096, 7168, 128, "e4m3", "ue8m0", "row", False, 2,
+                   "normal, 0.1% x100 outliers", op="rmsnorm"),
     "pb2": Workload("pb2", 4096, 7168, 128, "e4m3", "fp32", "row", False, 2,
                     "normal, 0.1% x100 outliers", op="block"),
     "pc2": Workload("pc2", 4096, 7168, 4096, "e4m3", "fp32", "row", False, 2,
@@ -192,6 +200,14 @@ def make_input(w: Workload, M: int | None = None) -> np.ndarray:
             x[den_rows] = sign | mant
         return x
     raise ValueError(f"unknown distribution {w.dist!r}")
+
+
+def make_gain(w: Workload) -> np.ndarray:
+    """RMSNorm gain for a workload: 1 + 0.1 N(0, 1) per channel, as BF16
+    bits, from a seed of its own (the input's seed + 1000)."""
+    rng = np.random.Generator(np.random.PCG64(w.seed + 1000))
+    g = 1.0 + 0.1 * rng.standard_normal(w.K, dtype=np.float32)
+    return f32_to_bf16_bits(g.astype(np.float32))
 
 
 def random_bf16(seed: int, rows: int, cols: int, scale: float = 1.0

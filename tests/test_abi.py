@@ -242,6 +242,36 @@ def test_per_channel_noalloc_validation(lib, name, kw, want):
     assert call_na(lib, **kw) == want
 
 
+def call_rms(lib, *, x=A, w=WS, M=4, K=256, ld_x=256, eps=1e-6, group=128,
+             fmt=0, mode=0, layout=0, codes=B, ld_codes=256, scales=C,
+             ld_scales=2):
+    return lib.tk_rmsnorm_per_token_cast(x, w, M, K, ld_x, eps, group, fmt,
+                                         mode, layout, codes, ld_codes,
+                                         scales, ld_scales, None)
+
+
+RMS_CASES = [
+    ("bad group", dict(group=48), INVALID),
+    ("negative eps", dict(eps=-1e-6), INVALID),
+    ("nan eps", dict(eps=float("nan")), INVALID),
+    ("inf eps", dict(eps=float("inf")), INVALID),
+    ("ld_x < K", dict(ld_x=128), INVALID),
+    ("scales too narrow", dict(ld_scales=1), INVALID),
+    ("null gain", dict(w=None), INVALID),
+    ("gain misaligned", dict(w=WS + 8), MISALIGNED),
+    ("x misaligned", dict(x=A + 8), MISALIGNED),
+    ("row longer than a stage", dict(K=8192 + 128, ld_x=8320, ld_codes=8320,
+                                     ld_scales=65), UNSUPPORTED),
+    ("empty batch", dict(M=0, x=None, w=None, codes=None, scales=None), OK),
+    ("zero eps allowed", dict(M=0, eps=0.0), OK),
+]
+
+
+@pytest.mark.parametrize("name,kw,want", RMS_CASES, ids=[c[0] for c in RMS_CASES])
+def test_rmsnorm_validation(lib, name, kw, want):
+    assert call_rms(lib, **kw) == want
+
+
 def test_per_channel_workspace_size(lib):
     # maxima for K rounded up to 128 channels + one counter per 128 (16-B units)
     assert tk.tk_per_channel_workspace_bytes(256) == 4 * 256 + 16
