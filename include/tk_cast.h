@@ -186,13 +186,13 @@ TK_API tk_status tk_per_token_cast_back(const void *x, int64_t M, int64_t K,
  * and Sennrich, "Root Mean Square Layer Normalization", 2019):
  *   y[m, k] = w[k] * x[m, k] / sqrt(eps + (1/K) * sum_j x[m, j]^2)
  * then y is cast exactly as tk_per_token_cast casts a row (no BF16
- * intermediate).  The kernel works in IEEE fp32: the sum of squares by
- * fused multiply-adds in a fixed order, rstd = 1 / sqrt(sum / K + eps)
- * with each step one correctly rounded operation, and y = RN((x * w) *
- * rstd), where x * w is exact.  Against y formed exactly, y is within about
- * (log2(K) + 8) fp32 ulps, so scales can differ from an exact evaluation by
- * that many ulps (fp32 mode; power-of-two scales only near a power of two)
- * and a small fraction of codes by one step.
+ * intermediate).  The kernel works in fp32: the sum of squares by fused
+ * multiply-adds in a fixed order, rstd = rsqrtf(sum * RN(1/K) + eps), and
+ * y = RN((x * w) * rstd), where x * w is exact.  Against y formed exactly,
+ * y is within about 25 fp32 ulps (K <= 8192), so fp32 scales can differ
+ * from an exact evaluation by that many ulps (power-of-two scales only
+ * next to a power of two), and a code by one step where the exact quotient
+ * lies that close to a rounding midpoint.
  *
  *   x         BF16 [M][ld_x], K values per row; K <= 8192 (one row per
  *             pipeline stage; TK_ERR_UNSUPPORTED beyond).

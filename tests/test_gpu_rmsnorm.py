@@ -3,12 +3,13 @@
 The kernel computes RMSNorm in fp32 (one fixed summation order, IEEE steps)
 and the oracle in double rounded once, so the compare is a tolerance one
 (tests/gpu_util.check_close).  SCALE_ULPS follows from the kernel's
-arithmetic: a lane adds at most 48 squares in order (47 roundings), the warp
-tree 5 more and the group 5 more, then the division by K, the addition of
-eps, the square root (which halves the relative error of its operand) and
-the reciprocal, and the product by rstd: at most about 0.5 * 59 + 3.5 = 33
-ulps between the kernel's y and exact y, and one more for the oracle's
-rounding; 40 leaves room.  So:
+arithmetic: a lane keeps two sums of at most 24 squares each (23 roundings),
+adds them (1), the warp tree adds 5 more and the group 5 more, then the
+product by RN(1/K) (2 with the rounding of 1/K) and the addition of eps (1):
+at most 37 ulps on the mean square; rsqrtf halves that and adds its own
+error (at most 2 ulps), and the product by rstd one more: about 22 ulps
+between the kernel's y and exact y, and one more for the oracle's rounding;
+40 leaves room.  So:
   * fp32 scales within SCALE_ULPS ulps; UE8M0 / power-of-two scales equal
     except within SCALE_ULPS ulps of a power of two;
   * a code may differ only by one step, and only where the oracle's y / s
