@@ -367,6 +367,39 @@ __device__ __forceinline__ void quotient2(uint32_t w, uint64_t s2, uint64_t inv2
   }
 }
 
+// Widened pair of the BF16 word w: element 0 in the low half.
+__device__ __forceinline__ uint64_t widen_pair(uint32_t w) {
+  return pack_f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ float lo_of(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_of(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// The larger of |a|, |b| and c (c >= 0), one three-input max.
+__device__ __forceinline__ float max_abs2(float c, float a, float b) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(c), "f"(fabsf(a)), "f"(fabsf(b)));
+  return d;
+}
+
 // quotient2's reciprocal operand for a scale: 2^-k for power-of-two
 // scales, the negated reciprocal for fp32 scales.
 template <bool POW2>
