@@ -275,6 +275,47 @@ def test_nondefault_stream_and_tensor_api():
     assert np.array_equal(hc.numpy(), rc)
 
 
+@pytest.mark.parametrize("fmt,scale,layout,K,group", [
+    ("e4m3", "ue8m0", "row", 7168, 128),
+    ("e4m3", "fp32", "transposed", 1024, 32),
+    ("e2m1", "ue8m0", "transposed", 272, 16),     # 136-byte code rows
+    ("e2m1", "pow2", "row", 272, 16),
+])
+def test_host_buffers_match_device_path(fmt, scale, layout, K, group):
+    """Host tensors in, host tensors out (copies inside the call): the
+    results must equal the device-tensor call's bit for bit, including E2M1
+    code rows whose device stride is padded to 16 bytes."""
+    import torch
+    M = 1613
+    bits = random_bf16(21, M, K, scale=4.0)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    dc, ds = tk.per_token_cast(x.cuda(), group=group, fmt=fmt, scale=scale,
+                               layout=layout)
+    hc, hs = tk.per_token_cast(x.pin_memory(), group=group, fmt=fmt,
+                               scale=scale, layout=layout)
+    torch.cuda.synchronize()
+    assert hc.device.type == "cpu" and hs.device.type == "cpu"
+    assert np.array_equal(hc.numpy(), dc.cpu().numpy())
+    if layout == "row":
+        assert np.array_equal(hs.numpy().view(np.uint32),
+                              ds.cpu().numpy().view(np.uint32))
+    else:
+        assert np.array_equal(hs.numpy().view(np.uint32)[:, :M],
+                              ds.cpu().numpy().view(np.uint32)[:, :M])
+    # the fused SwiGLU host path, same check
+    bits2 = random_bf16(22, M, 2 * K)
+    x2 = torch.from_numpy(bits2.view(np.int16)).view(torch.bfloat16)
+    dc, ds = tk.swiglu_per_token_cast(x2.cuda(), group=group, fmt=fmt,
+                                      scale=scale, layout=layout)
+    hc, hs = tk.swiglu_per_token_cast(x2.pin_memory(), group=group, fmt=fmt,
+                                      scale=scale, layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(hc.numpy(), dc.cpu().numpy())
+    n = M if layout == "transposed" else None
+    assert np.array_equal(hs.numpy().view(np.uint32)[..., :n],
+                          ds.cpu().numpy().view(np.uint32)[..., :n])
+
+
 def test_bf16_input_values_roundtrip():
     """Sanity: the decoded codes times the scales approximate the input."""
     import torch
