@@ -74,7 +74,7 @@ def test_packed_kernels_use_the_negated_form():
     negated reciprocal (quotient2_inv) -- the form the checker compares."""
     src = open(CU).read()
     body = src[src.index("__device__ __forceinline__ void quotient2("):]
-    body = body[body.index("} else {"):body.index("quotient2_inv")]
+    body = body[body.index("} else {"):body.index("\n}\n")]
     seq = re.findall(r'"(xor\.b32|mul\.rn\.f32x2|fma\.rn\.f32x2) ([^;]*);', body)
     assert seq == [("xor.b32", "n, %2, 0x80008000"),
                    ("mul.rn.f32x2", "q0, nx, %4"),
@@ -83,6 +83,24 @@ def test_packed_kernels_use_the_negated_form():
     assert '"r"(w), "l"(s2), "l"(inv2)' in body
     inv = src[src.index("float quotient2_inv("):]
     assert "return POW2 ? g.inv : -g.inv;" in inv[:200]
+
+
+def test_fp32_input_paths_use_the_negated_form():
+    """The SwiGLU and RMSNorm casts run the same negated-operand sequence
+    on values they form negated (-y), with the negated reciprocal."""
+    src = open(os.path.join(os.path.dirname(CU), "tk_cast.cu")).read()
+    sw = src[src.index("__device__ __forceinline__ void cast_chunk("):]
+    sw = sw[:sw.index("\n}\n")]
+    assert "const uint64_t ni = pack_f32x2(-gs.inv, -gs.inv);" in sw
+    assert "const uint64_t q0 = fmul2(ny[i], ni);" in sw
+    assert "r = ffma2(ffma2(q0, s2, ny[i]), ni, q0);" in sw
+    assert "ny[i] = pack_f32x2(-v0, -v1);" in sw              # slow path
+    rms = src[src.index("__device__ __forceinline__ void rms_chunk("):]
+    rms = rms[:rms.index("\n}\n")]
+    assert "const float f = POW2 ? rstd : -rstd;" in rms      # -y for fp32 scales
+    assert "const float iv = quotient2_inv<POW2>(gs);" in rms
+    assert "const uint64_t q0 = fmul2(y2[i], i2);" in rms
+    assert "r = ffma2(ffma2(q0, s2, y2[i]), i2, q0);" in rms
 
 
 @pytest.mark.parametrize("fmt_max", ["448", "6"])
