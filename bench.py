@@ -459,6 +459,8 @@ def run_gpu(args):
                            "frac_of_peak": round(gbps / peak, 4),
                            "bytes": other.bytes["total"],
                            "l2": other.l2_note(l2)}
+            if not args.no_cpu_baseline:     # the oracle timed beside it
+                table[name]["cpu_oracle"] = cpu_baseline(other.w, 1.0)
             del other
         result["per_config"] = table
 
@@ -509,30 +511,61 @@ def run_e2e(torch, tk, w, steps, device, world):
 
 # ------------------------------------------------------------- CPU arm
 
+def _oracle_op(w, threads):
+    """(prepare, run) for the oracle of a workload's op on a block of rows:
+    prepare(bits) builds the op's inputs (for dequantization: the oracle's
+    own codes and scales, outside the timed part), run(inputs) runs it."""
+    import oracle
+    fmt = oracle.FMT_E4M3 if w.fmt == "e4m3" else oracle.FMT_E2M1
+    mode = {"fp32": oracle.SCALE_FP32, "pow2": oracle.SCALE_FP32_POW2,
+            "ue8m0": oracle.SCALE_UE8M0}[w.scale]
+    layout = (oracle.LAYOUT_ROW_MAJOR if w.layout == "row"
+              else oracle.LAYOUT_TRANSPOSED)
+    same = (lambda bits: bits)
+    if w.op == "dequant":
+        def prep(bits):
+            return oracle.per_token_cast(bits, w.K, w.group, fmt, mode, layout,
+                                         threads=threads)
+        return prep, lambda cs: oracle.per_token_dequant(
+            cs[0], cs[1], w.K, w.group, fmt, mode, layout, threads=threads)
+    if w.op == "cast_back":
+        return same, lambda b: oracle.per_token_cast_back(
+            b, w.K, w.group, fmt, mode, threads=threads)
+    if w.op == "block":
+        return same, lambda b: oracle.per_block_cast(b, w.K, 128, fmt, mode,
+                                                     threads=threads)
+    if w.op == "channel":
+        return same, lambda b: oracle.per_channel_cast(b, w.K, fmt, mode,
+                                                       threads=threads)
+    if w.op == "rmsnorm":
+        gain = make_gain(w)
+        return same, lambda b: oracle.rmsnorm_per_token_cast(
+            b, gain, w.K, w.eps, w.group, fmt, mode, layout, threads=threads)
+    fn = oracle.swiglu_per_token_cast if w.swiglu else oracle.per_token_cast
+    return same, lambda b: fn(b, w.K, w.group, fmt, mode, layout,
+                              threads=threads)
+
+
 def cpu_baseline(w, seconds: float):
     """The oracle as it stands, on all host cores, over whole passes of the
     workload (or a leading block of rows when one pass would exceed the
     budget); GB/s over the same algorithmic bytes."""
     import oracle
     threads = oracle.host_threads()
-    fmt = oracle.FMT_E4M3 if w.fmt == "e4m3" else oracle.FMT_E2M1
-    mode = {"fp32": oracle.SCALE_FP32, "pow2": oracle.SCALE_FP32_POW2,
-            "ue8m0": oracle.SCALE_UE8M0}[w.scale]
-    layout = (oracle.LAYOUT_ROW_MAJOR if w.layout == "row"
-              else oracle.LAYOUT_TRANSPOSED)
-    fn = oracle.swiglu_per_token_cast if w.swiglu else oracle.per_token_cast
+    prep, run = _oracle_op(w, threads)
     # probe on a small block to size the sample
     probe_rows = max(threads, min(w.M, 256))
     bits = make_input(w, M=probe_rows) if probe_rows < w.M else make_input(w)
+    probe = prep(bits[:probe_rows])
     t0 = time.perf_counter()
-    fn(bits[:probe_rows], w.K, w.group, fmt, mode, layout, threads=threads)
+    run(probe)
     per_row = (time.perf_counter() - t0) / probe_rows
     rows = int(min(w.M, max(probe_rows, seconds / max(per_row, 1e-9))))
-    sample = make_input(w, M=rows) if rows < w.M else make_input(w)
+    sample = prep(make_input(w, M=rows) if rows < w.M else make_input(w))
     passes, elapsed = 0, 0.0
     t0 = time.perf_counter()
     while True:
-        fn(sample, w.K, w.group, fmt, mode, layout, threads=threads)
+        run(sample)
         passes += 1
         elapsed = time.perf_counter() - t0
         if elapsed >= min(seconds, 3.0) or passes >= 1000:
