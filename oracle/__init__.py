@@ -85,6 +85,12 @@ def _configure(lib):
                                                   ctypes.c_float, i, i, i, i,
                                                   p, i64, p, i64]
     lib.oracle_rmsnorm_per_token_cast.restype = i
+    lib.oracle_per_block_dequant.argtypes = [p, i64, p, i64, i64, i64, i64,
+                                             i, i, i, i, p, i64]
+    lib.oracle_per_block_dequant.restype = i
+    lib.oracle_per_channel_dequant.argtypes = [p, i64, p, i64, i64, i64, i,
+                                               i, i, p, i64]
+    lib.oracle_per_channel_dequant.restype = i
     lib.oracle_per_block_cast.argtypes = [p, i64, i64, i64, i, i64, i64, i, i,
                                           p, i64, p, i64]
     lib.oracle_per_block_cast.restype = i
@@ -418,6 +424,51 @@ def per_channel_cast(x_bits: np.ndarray, K: int, fmt: int, mode: int, *,
     _check([work(0)] if threads == 1 else
            list(_executor(threads).map(work, range(threads))))
     return codes, scales
+
+
+def _dequant_out(M, K, out_fp32):
+    return np.zeros((M, K), np.float32 if out_fp32 else np.uint16)
+
+
+def per_block_dequant(codes: np.ndarray, scales: np.ndarray, K: int,
+                      block: int, fmt: int, mode: int, *,
+                      out_fp32: bool = False, threads: int = 1):
+    """Oracle per-block dequantization (codes and scales as per_block_cast
+    returns them): fp32, or BF16 bits."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales)
+    M = codes.shape[0]
+    y = _dequant_out(M, K, out_fp32)
+    ld_s = scales.strides[0] // 4
+
+    def work(a, b):
+        return lib.oracle_per_block_dequant(
+            _ptr(codes), codes.strides[0], _ptr(scales), ld_s, a, b, K, block,
+            fmt, mode, int(out_fp32), _ptr(y), K)
+
+    _split(M, threads, work)
+    return y
+
+
+def per_channel_dequant(codes: np.ndarray, scales: np.ndarray, K: int,
+                        fmt: int, mode: int, *, out_fp32: bool = False,
+                        threads: int = 1):
+    """Oracle per-channel dequantization (codes and the scale vector as
+    per_channel_cast returns them): fp32, or BF16 bits."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales)
+    M = codes.shape[0]
+    y = _dequant_out(M, K, out_fp32)
+
+    def work(a, b):
+        return lib.oracle_per_channel_dequant(
+            _ptr(codes), codes.strides[0], _ptr(scales), a, b, K, fmt, mode,
+            int(out_fp32), _ptr(y), K)
+
+    _split(M, threads, work)
+    return y
 
 
 def swiglu_value(gate: float, up: float) -> float:

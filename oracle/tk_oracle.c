@@ -707,6 +707,71 @@ int oracle_per_channel_cast(const uint16_t *x, int64_t M, int64_t K,
     return OR_OK;
 }
 
+/* --------------------------------- per-block and per-channel dequantization */
+
+/*
+ * TileKernels README, "Features": the per-block and per-channel casts come
+ * with dequantization.  Its element step is the per-token one: the code's
+ * exact value times the scale of the code's block (or channel), one IEEE
+ * fp32 multiply, stored as fp32 or rounded to BF16 (nearest even); codes
+ * and scales are laid out as oracle_per_block_cast / oracle_per_channel_cast
+ * write them.  Rows [m_begin, m_end) are processed; y row m at y + m*ld_y
+ * elements of the output type.
+ */
+static float code_value(const uint8_t *code_row, int64_t k, int fmt)
+{
+    if (fmt == OR_FMT_E4M3)
+        return e4m3_decode(code_row[k]);
+    uint8_t byte = code_row[k / 2];
+    return e2m1_decode((uint8_t)((k & 1) ? byte >> 4 : byte & 0xF));
+}
+
+static void put_output(void *y, int64_t at, int out_fp32, float value)
+{
+    if (out_fp32)
+        ((float *)y)[at] = value;
+    else
+        ((uint16_t *)y)[at] = float_to_bf16_bits(value);
+}
+
+int oracle_per_block_dequant(const uint8_t *codes, int64_t ld_codes,
+                             const void *scales, int64_t ld_scales,
+                             int64_t m_begin, int64_t m_end, int64_t K,
+                             int block, int fmt, int mode, int out_fp32,
+                             void *y, int64_t ld_y)
+{
+    if (block != 16 && block != 32 && block != 64 && block != 128)
+        return OR_BAD_ARG;
+    int rc = check_tile_args(m_end, K, fmt, mode);
+    if (rc != OR_OK)
+        return rc;
+    for (int64_t m = m_begin; m < m_end; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            float s = read_scale(scales, ld_scales, mode, OR_LAYOUT_ROW_MAJOR,
+                                 m / block, k / block);
+            put_output(y, m * ld_y + k, out_fp32,
+                       code_value(codes + m * ld_codes, k, fmt) * s);
+        }
+    return OR_OK;
+}
+
+int oracle_per_channel_dequant(const uint8_t *codes, int64_t ld_codes,
+                               const void *scales, int64_t m_begin,
+                               int64_t m_end, int64_t K, int fmt, int mode,
+                               int out_fp32, void *y, int64_t ld_y)
+{
+    int rc = check_tile_args(m_end, K, fmt, mode);
+    if (rc != OR_OK)
+        return rc;
+    for (int64_t m = m_begin; m < m_end; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            float s = read_scale(scales, 0, mode, OR_LAYOUT_ROW_MAJOR, 0, k);
+            put_output(y, m * ld_y + k, out_fp32,
+                       code_value(codes + m * ld_codes, k, fmt) * s);
+        }
+    return OR_OK;
+}
+
 /* ------------------------------------------- element-level hooks for pins */
 
 /* Saturating RNE encode of n fp32 values (the code step of the cast alone). */

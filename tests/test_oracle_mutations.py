@@ -93,6 +93,11 @@ TILE_MUTATIONS = {
     "tile_nibble_order": ("if (col % 2 == 0)", "if (col % 2 == 1)"),
     "tile_scale_multiplied": ("bf16_bits_to_float(x[m * ld_x + k]) / sc.s);",
                               "bf16_bits_to_float(x[m * ld_x + k]) * sc.s);"),
+    "block_dequant_scale_transposed": ("m / block, k / block);", "k / block, m / block);"),
+    "channel_dequant_divides": ("code_value(codes + m * ld_codes, k, fmt) * s);\n        }\n    return OR_OK;\n}\n\n/* ---",
+                                "code_value(codes + m * ld_codes, k, fmt) / s);\n        }\n    return OR_OK;\n}\n\n/* ---"),
+    "dequant_e2m1_nibble_order": ("return e2m1_decode((uint8_t)((k & 1) ? byte >> 4 : byte & 0xF));\n}\n\nstatic void put_output",
+                                  "return e2m1_decode((uint8_t)((k & 1) ? byte & 0xF : byte >> 4));\n}\n\nstatic void put_output"),
 }
 
 

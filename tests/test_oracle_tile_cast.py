@@ -255,3 +255,117 @@ def test_per_channel_without_rows_writes_nothing():
     oracle.per_channel_cast(np.zeros((0, 16), np.uint16), 16, oracle.FMT_E4M3,
                             oracle.SCALE_FP32, codes=codes, scales=s)
     assert (s == 7.0).all()
+
+
+# ------------------------------------------------------- dequantization
+
+def _codes_without_nan(rng, M, K, fname):
+    nb = K if fname == "e4m3" else K // 2
+    c = rng.integers(0, 256, size=(M, nb), dtype=np.uint8)
+    if fname == "e4m3":
+        c[(c & 0x7F) == 0x7F] = 0x35
+    return c
+
+
+def _scale_words(rng, n_rows, n, mname):
+    """Random scale rows: positive fp32 values spanning many binades, or
+    UE8M0 bytes 1..254 packed four per word (unused bytes zero)."""
+    if mname == "ue8m0":
+        b = np.zeros((n_rows, -(-n // 4) * 4), np.uint8)
+        b[:, :n] = rng.integers(1, 255, size=(n_rows, n), dtype=np.uint8)
+        return b.view(np.int32), b[:, :n].astype(np.float64)
+    v = np.exp2(rng.uniform(-30, 30, size=(n_rows, n))).astype(np.float32)
+    return v, v.astype(np.float64)
+
+
+def _want(vals, bf16_out):
+    y = vals.astype(np.float32)            # the exact product, rounded once
+    if bf16_out:
+        from precision_quantization_token_gb300.inputs import f32_to_bf16_bits
+        return f32_to_bf16_bits(y)
+    return y
+
+
+@pytest.mark.parametrize("fname,fmt", FMTS)
+@pytest.mark.parametrize("mname,mode", [("fp32", oracle.SCALE_FP32),
+                                        ("ue8m0", oracle.SCALE_UE8M0)])
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_block_dequant_is_one_multiply(fname, fmt, mname, mode, bf16_out):
+    M, K, block = 70, 96, 32
+    rng = np.random.default_rng(31)
+    codes = _codes_without_nan(rng, M, K, fname)
+    words, sval = _scale_words(rng, -(-M // block), -(-K // block), mname)
+    if mname == "ue8m0":
+        sval = np.exp2(sval - 127)
+    y = oracle.per_block_dequant(codes, words, K, block, fmt, mode,
+                                 out_fp32=not bf16_out)
+    from bruteforce import decode
+    v = decode(unpack(codes, fname), fname)
+    s = sval[np.arange(M)[:, None] // block, np.arange(K)[None, :] // block]
+    assert np.array_equal(y.view(np.uint16 if bf16_out else np.uint32),
+                          _want(v * s, bf16_out).view(np.uint16 if bf16_out else np.uint32))
+
+
+@pytest.mark.parametrize("fname,fmt", FMTS)
+@pytest.mark.parametrize("mname,mode", [("fp32", oracle.SCALE_FP32),
+                                        ("ue8m0", oracle.SCALE_UE8M0)])
+@pytest.mark.parametrize("bf16_out", [False, True])
+def test_channel_dequant_is_one_multiply(fname, fmt, mname, mode, bf16_out):
+    M, K = 33, 80
+    rng = np.random.default_rng(32)
+    codes = _codes_without_nan(rng, M, K, fname)
+    words, sval = _scale_words(rng, 1, K, mname)
+    if mname == "ue8m0":
+        sval = np.exp2(sval - 127)
+    y = oracle.per_channel_dequant(codes, words[0], K, fmt, mode,
+                                   out_fp32=not bf16_out)
+    from bruteforce import decode
+    v = decode(unpack(codes, fname), fname)
+    assert np.array_equal(y.view(np.uint16 if bf16_out else np.uint32),
+                          _want(v * sval[0][None, :], bf16_out).view(
+                              np.uint16 if bf16_out else np.uint32))
+
+
+@pytest.mark.parametrize("fname,fmt", FMTS)
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_one_row_block_dequant_is_per_token_dequant(fname, fmt, mname, mode):
+    K = 5 * 32
+    bits = bf16_matrix(1, K, seed=33)
+    codes, scales = oracle.per_block_cast(bits, K, 32, fmt, mode)
+    a = oracle.per_block_dequant(codes, scales, K, 32, fmt, mode)
+    b = oracle.per_token_dequant(codes, scales, K, 32, fmt, mode,
+                                 oracle.LAYOUT_ROW_MAJOR)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("fname,fmt", FMTS)
+@pytest.mark.parametrize("mname,mode", MODES)
+def test_dequant_inverts_the_cast_within_half_a_step(fname, fmt, mname, mode):
+    """|x - dequant(cast(x))| <= half the code gap at the decoded value,
+    times the scale, plus |x| 2^-23 (the fp32 quotient's rounding)."""
+    from bruteforce import decode_table
+    M, K = 150, 272
+    bits = bf16_matrix(M, K, seed=34)
+    x = as_f32(bits).astype(np.float64)
+    table = decode_table(fname)
+    gaps = np.diff(table)
+    for kind in ("block", "channel"):
+        if kind == "block":
+            codes, scales = oracle.per_block_cast(bits, K, 128, fmt, mode)
+            y = oracle.per_block_dequant(codes, scales, K, 128, fmt, mode,
+                                         out_fp32=True).astype(np.float64)
+        else:
+            codes, scales = oracle.per_channel_cast(bits, K, fmt, mode)
+            y = oracle.per_channel_dequant(codes, scales, K, fmt, mode,
+                                           out_fp32=True).astype(np.float64)
+        v = decode(unpack(codes, fname), fname)
+        s = np.divide(y, v, out=np.zeros_like(y), where=v != 0)
+        # the scale of each element: recover it from a nonzero neighbour's
+        # ratio is fragile; bound with the largest gap of the format instead
+        # where the code is zero
+        idx = np.searchsorted(table, np.abs(v))
+        gap = np.where(idx < gaps.size, gaps[np.minimum(idx, gaps.size - 1)],
+                       gaps[-1])
+        bound = 0.5 * gap * np.abs(s) + np.abs(x) * 2.0 ** -23
+        ok = (v == 0) | (np.abs(x - y) <= bound * (1 + 1e-12))
+        assert ok.all(), (kind, np.argwhere(~ok)[:3])
