@@ -229,8 +229,10 @@ class GpuWorkload:
         bits = make_input(w)
         x0 = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(device)
         row_bytes = w.K if w.fmt == "e4m3" else w.K // 2
-        if w.op == "block":
+        if w.op in ("block", "block_dequant"):
             shape, dt = tk.block_scale_shape(w.M, w.K, w.scale)
+        elif w.op == "channel_dequant":
+            shape, dt = tk.channel_scale_shape(w.K, w.scale)
         elif w.op == "channel":
             shape, dt = tk.channel_scale_shape(w.K, w.scale)
             self.workspace = torch.zeros(tk.tk_per_channel_workspace_bytes(w.K),
@@ -241,14 +243,19 @@ class GpuWorkload:
             g = make_gain(w)
             self.gain = torch.from_numpy(g.view(np.int16)).view(
                 torch.bfloat16).to(device)
-        if w.op == "dequant":
+        if w.op.endswith("dequant"):
             # the codes and scales to dequantize come from one (untimed) cast
-            c0, s0 = tk.per_token_cast(x0, w.group, w.fmt, w.scale, w.layout)
+            if w.op == "block_dequant":
+                c0, s0 = tk.per_block_cast(x0, w.fmt, w.scale)
+            elif w.op == "channel_dequant":
+                c0, s0 = tk.per_channel_cast(x0, w.fmt, w.scale)
+            else:
+                c0, s0 = tk.per_token_cast(x0, w.group, w.fmt, w.scale, w.layout)
             torch.cuda.synchronize()
             del x0
         self.sets = []
         for i in range(self.copies):
-            if w.op == "dequant":
+            if w.op.endswith("dequant"):
                 codes = c0 if i == 0 else c0.clone()
                 scales = s0 if i == 0 else s0.clone()
                 y = torch.empty((w.M, w.K), dtype=torch.bfloat16, device=device)
@@ -280,6 +287,18 @@ class GpuWorkload:
                                       w.group, tk.FMT[w.fmt],
                                       tk.SCALE[w.scale], b.data_ptr(),
                                       b.stride(0), stream_handle)
+        elif w.op == "block_dequant":
+            tk.tk_per_block_dequant(a.data_ptr(), a.stride(0), b.data_ptr(),
+                                    b.stride(0), w.M, w.K, tk.FMT[w.fmt],
+                                    tk.SCALE[w.scale], c.data_ptr(),
+                                    c.stride(0), tk.OUT_DTYPE["bf16"],
+                                    stream_handle)
+        elif w.op == "channel_dequant":
+            tk.tk_per_channel_dequant(a.data_ptr(), a.stride(0), b.data_ptr(),
+                                      w.M, w.K, tk.FMT[w.fmt],
+                                      tk.SCALE[w.scale], c.data_ptr(),
+                                      c.stride(0), tk.OUT_DTYPE["bf16"],
+                                      stream_handle)
         elif w.op == "rmsnorm":
             tk.tk_rmsnorm_per_token_cast(a.data_ptr(), self.gain.data_ptr(),
                                          w.M, w.K, a.stride(0), w.eps,
@@ -528,6 +547,17 @@ def _oracle_op(w, threads):
                                          threads=threads)
         return prep, lambda cs: oracle.per_token_dequant(
             cs[0], cs[1], w.K, w.group, fmt, mode, layout, threads=threads)
+    if w.op in ("block_dequant", "channel_dequant"):
+        if w.op == "block_dequant":
+            return (lambda bits: oracle.per_block_cast(bits, w.K, 128, fmt, mode,
+                                                       threads=threads),
+                    lambda cs: oracle.per_block_dequant(cs[0], cs[1], w.K, 128,
+                                                        fmt, mode,
+                                                        threads=threads))
+        return (lambda bits: oracle.per_channel_cast(bits, w.K, fmt, mode,
+                                                     threads=threads),
+                lambda cs: oracle.per_channel_dequant(cs[0], cs[1], w.K, fmt,
+                                                      mode, threads=threads))
     if w.op == "cast_back":
         return same, lambda b: oracle.per_token_cast_back(
             b, w.K, w.group, fmt, mode, threads=threads)

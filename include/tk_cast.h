@@ -272,6 +272,36 @@ TK_API tk_status tk_per_channel_cast(const void *x, int64_t M, int64_t K,
                                      size_t workspace_bytes, void *stream);
 
 /*
+ * tk_per_block_dequant, tk_per_channel_dequant -- dequantization of the
+ * per-block / per-channel casts' output (TileKernels README, "Features":
+ * "per-block, and per-channel FP8/FP4 casting and dequantization"):
+ *   y[m, k] = value(code[m, k]) * scale(block of (m, k), or channel k)
+ * as tk_per_token_dequant computes it (exact decode, one IEEE fp32
+ * multiply, BF16 nearest-even or fp32 out; a UE8M0 byte e is 2^(e-127)).
+ *
+ *   codes     uint8 [M][ld_codes] as the casts write them (K % 16 == 0),
+ *             16-byte aligned, ld_codes a multiple of 16.  Per-block E2M1
+ *             codes are read up to the next 16-byte boundary of each row
+ *             (as tk_per_token_dequant does): the buffer spans M * ld_codes.
+ *   scales    per-block: as tk_per_block_cast writes them, with its
+ *             ld_scales (4-byte aligned); per-channel: the scale vector,
+ *             16-byte aligned.
+ *   y         [M][ld_y] elements of out_dtype (tk_out_dtype), 16-byte
+ *             aligned, ld_y * sizeof(element) a multiple of 16, ld_y >= K.
+ */
+TK_API tk_status tk_per_block_dequant(const void *codes, int64_t ld_codes,
+                                      const void *scales, int64_t ld_scales,
+                                      int64_t M, int64_t K, int fmt, int mode,
+                                      void *y, int64_t ld_y, int out_dtype,
+                                      void *stream);
+
+TK_API tk_status tk_per_channel_dequant(const void *codes, int64_t ld_codes,
+                                        const void *scales, int64_t M,
+                                        int64_t K, int fmt, int mode, void *y,
+                                        int64_t ld_y, int out_dtype,
+                                        void *stream);
+
+/*
  * tk_per_channel_cast_noalloc -- tk_per_channel_cast without a caller
  * workspace.  The pages have no counterpart: it is an interface for
  * callers that cannot allocate device memory where they call the cast (a

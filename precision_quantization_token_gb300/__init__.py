@@ -22,6 +22,10 @@ Low level (same names and arguments as the C ABI, raw pointers and sizes):
     tk_per_channel_cast(x_ptr, M, K, ld_x, fmt, mode, codes_ptr, ld_codes,
                         scales_ptr, workspace_ptr, workspace_bytes, stream)
     tk_per_channel_workspace_bytes(K)
+    tk_per_block_dequant(codes_ptr, ld_codes, scales_ptr, ld_scales, M, K,
+                         fmt, mode, y_ptr, ld_y, out_dtype, stream)
+    tk_per_channel_dequant(codes_ptr, ld_codes, scales_ptr, M, K, fmt, mode,
+                           y_ptr, ld_y, out_dtype, stream)
     tk_per_channel_cast_noalloc(x_ptr, M, K, ld_x, fmt, mode, codes_ptr,
                                 ld_codes, scales_ptr, stream)
 
@@ -34,6 +38,8 @@ Tensor level (allocates outputs with torch):
     codes, scales = rmsnorm_per_token_cast(x, w, eps=1e-6, group=128, ...)
     codes, scales = per_block_cast(x, fmt="e4m3", scale="fp32")   # 128x128
     codes, scales = per_channel_cast(x, fmt="e4m3", scale="fp32")
+    y = per_block_dequant(codes, scales, K, fmt="e4m3", scale="fp32")
+    y = per_channel_dequant(codes, scales, K, fmt="e4m3", scale="fp32")
 
 Operation (TileKernels README, "Features"; aiwiki "TileKernels", section
 "Quantization"): per row and per group of 16/32/64/128 channels, amax, a
@@ -116,6 +122,12 @@ def load():
             lib.tk_per_channel_cast_noalloc.argtypes = [p, i64, i64, i64, i, i,
                                                         p, i64, p, p]
             lib.tk_per_channel_cast_noalloc.restype = i
+            lib.tk_per_block_dequant.argtypes = [p, i64, p, i64, i64, i64, i,
+                                                 i, p, i64, i, p]
+            lib.tk_per_block_dequant.restype = i
+            lib.tk_per_channel_dequant.argtypes = [p, i64, p, i64, i64, i, i,
+                                                   p, i64, i, p]
+            lib.tk_per_channel_dequant.restype = i
             lib.tk_per_channel_workspace_bytes.argtypes = [i64]
             lib.tk_per_channel_workspace_bytes.restype = ctypes.c_size_t
             lib.tk_get_device_fault.argtypes = [p, i]
@@ -205,6 +217,22 @@ def tk_per_channel_cast_noalloc(x_ptr, M, K, ld_x, fmt, mode, codes_ptr,
     _check(load().tk_per_channel_cast_noalloc(x_ptr, M, K, ld_x, fmt, mode,
                                               codes_ptr, ld_codes, scales_ptr,
                                               stream))
+
+
+def tk_per_block_dequant(codes_ptr, ld_codes, scales_ptr, ld_scales, M, K,
+                         fmt, mode, y_ptr, ld_y, out_dtype, stream=0) -> None:
+    """Raw-pointer call of the per-block dequantization."""
+    _check(load().tk_per_block_dequant(codes_ptr, ld_codes, scales_ptr,
+                                       ld_scales, M, K, fmt, mode, y_ptr,
+                                       ld_y, out_dtype, stream))
+
+
+def tk_per_channel_dequant(codes_ptr, ld_codes, scales_ptr, M, K, fmt, mode,
+                           y_ptr, ld_y, out_dtype, stream=0) -> None:
+    """Raw-pointer call of the per-channel dequantization."""
+    _check(load().tk_per_channel_dequant(codes_ptr, ld_codes, scales_ptr, M,
+                                         K, fmt, mode, y_ptr, ld_y, out_dtype,
+                                         stream))
 
 
 def tk_per_channel_workspace_bytes(K: int) -> int:
@@ -473,3 +501,42 @@ def per_channel_cast(x, fmt: str = "e4m3", scale: str = "fp32", *,
                         scales.data_ptr(), workspace.data_ptr(),
                         workspace.numel(), stream)
     return codes, scales
+
+
+def _dequant_out(torch, codes, K, out_dtype, out):
+    if out is None:
+        dt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+        out = torch.empty((codes.shape[0], K), dtype=dt, device=codes.device)
+    return out
+
+
+def per_block_dequant(codes, scales, K: int, fmt: str = "e4m3",
+                      scale: str = "fp32", out_dtype: str = "bf16", *,
+                      out=None, stream=None):
+    """Dequantize per-block codes [M, K or K/2] (uint8, CUDA) with the
+    scales per_block_cast returns: BF16 or fp32 [M, K]."""
+    import torch
+    out = _dequant_out(torch, codes, K, out_dtype, out)
+    if stream is None:
+        stream = torch.cuda.current_stream(codes.device).cuda_stream
+    tk_per_block_dequant(codes.data_ptr(), codes.stride(0), scales.data_ptr(),
+                         scales.stride(0), codes.shape[0], K, FMT[fmt],
+                         SCALE[scale], out.data_ptr(), out.stride(0),
+                         OUT_DTYPE[out_dtype], stream)
+    return out
+
+
+def per_channel_dequant(codes, scales, K: int, fmt: str = "e4m3",
+                        scale: str = "fp32", out_dtype: str = "bf16", *,
+                        out=None, stream=None):
+    """Dequantize per-channel codes [M, K or K/2] (uint8, CUDA) with the
+    scale vector per_channel_cast returns: BF16 or fp32 [M, K]."""
+    import torch
+    out = _dequant_out(torch, codes, K, out_dtype, out)
+    if stream is None:
+        stream = torch.cuda.current_stream(codes.device).cuda_stream
+    tk_per_channel_dequant(codes.data_ptr(), codes.stride(0),
+                           scales.data_ptr(), codes.shape[0], K, FMT[fmt],
+                           SCALE[scale], out.data_ptr(), out.stride(0),
+                           OUT_DTYPE[out_dtype], stream)
+    return out

@@ -29,6 +29,12 @@ tk_status fail_message(const char* what);
 
 const char* last_cuda_error();
 
+// Dequantization of per-block (128 x 128) codes on the per-token
+// dequantization pipeline; the caller has validated the arguments.
+tk_status block_dequant(const void* codes, int64_t ld_codes, const void* scales,
+                        int64_t ld_scales, int64_t M, int64_t K, int fmt, int mode, void* y,
+                        int64_t ld_y, int out_dtype, void* stream);
+
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }

@@ -434,6 +434,93 @@ tile_cast_kernel(const __grid_constant__ CUtensorMap map, const TileParams p) {
   }
 }
 
+// ------------------------------------------- per-channel dequantization
+// y = code value * its channel's scale (one IEEE fp32 multiply), BF16
+// (nearest even) or fp32 out.  An elementwise kernel: thread t of block
+// (bx, by) owns the 16-channel column chunk bx * kDequantThreads + t, loads
+// its 16 scales once, and walks rows by*R, (by + gridDim.y)*R, ... R at a
+// time (R code loads in flight per thread).  Codes decode with the exact
+// hardware conversions; each row chunk leaves as 32 B (BF16) or 64 B
+// (fp32).  (Per-block codes dequantize on the per-token pipeline instead:
+// there one scale serves a whole 16-channel chunk.)
+
+struct ChannelDequantParams {
+  const uint8_t* codes;      // row m at codes + m * ld_codes
+  int64_t ld_codes;
+  const uint8_t* scales;     // K fp32 words or K UE8M0 bytes, 16-byte aligned
+  uint8_t* y;                // row m at y + m * ld_y_bytes
+  int64_t ld_y_bytes;
+  int M;
+  int cpr;                   // 16-channel chunks per row
+  int ue8m0;
+  int y_fp32;
+};
+
+constexpr int kDequantThreads = 64;
+constexpr int kDequantRows = 4;            // rows per thread per step
+constexpr int kDequantCtasPerSm = 32;
+
+template <int FMT>
+__global__ void __launch_bounds__(kDequantThreads)
+channel_dequant_kernel(const ChannelDequantParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int c = (int)blockIdx.x * kDequantThreads + (int)threadIdx.x;
+  if (c >= p.cpr) return;
+  const int col = c * 16;
+  const int64_t code_off = FMT == TK_FMT_E4M3 ? col : col / 2;
+  float s[16];
+  if (p.ue8m0) {
+    const uint4 e = *reinterpret_cast<const uint4*>(p.scales + col);
+    const uint32_t w[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t b = (w[k / 4] >> (8 * (k % 4))) & 0xFFu;
+      s[k] = __uint_as_float(b ? b << 23 : 0x00400000u);   // 2^(b-127)
+    }
+  } else {
+    const float4* f = reinterpret_cast<const float4*>(p.scales) + col / 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 q = f[i];
+      s[4 * i] = q.x;
+      s[4 * i + 1] = q.y;
+      s[4 * i + 2] = q.z;
+      s[4 * i + 3] = q.w;
+    }
+  }
+  for (int r0 = (int)blockIdx.y * kDequantRows; r0 < p.M;
+       r0 += (int)gridDim.y * kDequantRows) {
+    uint4 raw[kDequantRows];
+#pragma unroll
+    for (int j = 0; j < kDequantRows; ++j) {
+      if (r0 + j >= p.M) break;
+      const uint8_t* at = p.codes + (int64_t)(r0 + j) * p.ld_codes + code_off;
+      if constexpr (FMT == TK_FMT_E4M3) {
+        raw[j] = *reinterpret_cast<const uint4*>(at);
+      } else {
+        const uint2 h = *reinterpret_cast<const uint2*>(at);
+        raw[j] = make_uint4(h.x, h.y, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kDequantRows; ++j) {
+      const int row = r0 + j;
+      if (row >= p.M) break;
+      float v[16];
+      if constexpr (FMT == TK_FMT_E4M3) {
+        decode16_e4m3(raw[j], v);
+      } else {
+        decode16_e2m1(make_uint2(raw[j].x, raw[j].y), v);
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], s[k]);
+      store_scaled16(p.y + (int64_t)row * p.ld_y_bytes + (int64_t)col * (p.y_fp32 ? 4 : 2),
+                     v, 1.0f, p.y_fp32 != 0);
+    }
+  }
+}
+
 // ------------------------------------------------------------ host side
 
 using TileKernel = void (*)(CUtensorMap, TileParams);
@@ -583,6 +670,64 @@ tk_status channel_scratch(void** out) {
   return TK_OK;
 }
 
+tk_status channel_dequant(const void* codes, int64_t ld_codes, const void* scales,
+                          int64_t M, int64_t K, int fmt, int mode, void* y, int64_t ld_y,
+                          int out_dtype, void* stream) {
+  const int64_t out_size = out_dtype == TK_OUT_FP32 ? 4 : 2;
+  ChannelDequantParams p = {};
+  p.codes = static_cast<const uint8_t*>(codes);
+  p.ld_codes = ld_codes;
+  p.scales = static_cast<const uint8_t*>(scales);
+  p.y = static_cast<uint8_t*>(y);
+  p.ld_y_bytes = ld_y * out_size;
+  p.M = (int)M;
+  p.cpr = (int)(K / 16);
+  p.ue8m0 = mode == TK_SCALE_UE8M0_PACKED ? 1 : 0;
+  p.y_fp32 = out_dtype == TK_OUT_FP32 ? 1 : 0;
+  void (*fn)(ChannelDequantParams) = fmt == TK_FMT_E4M3 ? channel_dequant_kernel<TK_FMT_E4M3>
+                                                        : channel_dequant_kernel<TK_FMT_E2M1>;
+  int sms = 0;
+  cudaError_t err = tk_internal::prepare_kernel(reinterpret_cast<const void*>(fn), 0, &sms);
+  if (err != cudaSuccess) return cuda_fail(err);
+  // x: the row's column chunks; y: row strides, an equal number per block,
+  // enough to fill every SM
+  const int64_t gx = (p.cpr + kDequantThreads - 1) / kDequantThreads;
+  const int64_t row_steps = (M + kDequantRows - 1) / kDequantRows;
+  const int64_t target = ((int64_t)sms * kDequantCtasPerSm + gx - 1) / gx;
+  const int64_t iters = (row_steps + target - 1) / target;
+  int64_t gy = (row_steps + iters - 1) / iters;
+  if (gy > 65535) gy = 65535;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = dependent_launch(attr, 1u, kDequantThreads, 0, stream);
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)gy);
+  err = cudaLaunchKernelEx(&cfg, fn, p);
+  if (err == cudaSuccess) err = cudaGetLastError();
+  return err == cudaSuccess ? TK_OK : cuda_fail(err);
+}
+
+tk_status check_dequant_args(int64_t M, int64_t K, int fmt, int mode, int64_t ld_codes,
+                             int64_t ld_y, int out_dtype) {
+  if (fmt != TK_FMT_E4M3 && fmt != TK_FMT_E2M1) return TK_ERR_INVALID_ARG;
+  if (mode < TK_SCALE_FP32 || mode > TK_SCALE_UE8M0_PACKED) return TK_ERR_INVALID_ARG;
+  if (out_dtype != TK_OUT_BF16 && out_dtype != TK_OUT_FP32) return TK_ERR_INVALID_ARG;
+  if (M < 0 || K <= 0 || K % 16 != 0) return TK_ERR_INVALID_ARG;
+  if (M > (int64_t(1) << 30) || K > (int64_t(1) << 28)) return TK_ERR_UNSUPPORTED;
+  const int64_t code_bytes = fmt == TK_FMT_E4M3 ? K : K / 2;
+  if (ld_codes < code_bytes || ld_y < K) return TK_ERR_INVALID_ARG;
+  return TK_OK;
+}
+
+tk_status check_dequant_pointers(const void* codes, int64_t ld_codes, const void* scales,
+                                 uintptr_t scale_align, const void* y, int64_t ld_y,
+                                 int out_dtype) {
+  if (codes == nullptr || scales == nullptr || y == nullptr) return TK_ERR_INVALID_ARG;
+  const int64_t out_size = out_dtype == TK_OUT_FP32 ? 4 : 2;
+  if (!aligned(codes, 16) || ld_codes % 16 != 0 || !aligned(scales, scale_align) ||
+      !aligned(y, 16) || (ld_y * out_size) % 16 != 0)
+    return TK_ERR_MISALIGNED;
+  return TK_OK;
+}
+
 }  // namespace
 
 namespace tk_internal {
@@ -676,6 +821,32 @@ tk_status tk_per_channel_cast_noalloc(const void* x, int64_t M, int64_t K, int64
   if (st != TK_OK) return st;
   return tk_per_channel_cast(x, M, K, ld_x, fmt, mode, codes, ld_codes, scales, scratch,
                              kNoAllocScratchBytes, stream);
+}
+
+tk_status tk_per_block_dequant(const void* codes, int64_t ld_codes, const void* scales,
+                               int64_t ld_scales, int64_t M, int64_t K, int fmt, int mode,
+                               void* y, int64_t ld_y, int out_dtype, void* stream) {
+  tk_status st = check_dequant_args(M, K, fmt, mode, ld_codes, ld_y, out_dtype);
+  if (st != TK_OK) return st;
+  const int64_t n_cb = (K + kTileCols - 1) / kTileCols;
+  if (ld_scales < (mode == TK_SCALE_UE8M0_PACKED ? (n_cb + 3) / 4 : n_cb))
+    return TK_ERR_INVALID_ARG;
+  if (M == 0) return TK_OK;
+  st = check_dequant_pointers(codes, ld_codes, scales, 4, y, ld_y, out_dtype);
+  if (st != TK_OK) return st;
+  return tk_internal::block_dequant(codes, ld_codes, scales, ld_scales, M, K, fmt, mode, y,
+                                   ld_y, out_dtype, stream);
+}
+
+tk_status tk_per_channel_dequant(const void* codes, int64_t ld_codes, const void* scales,
+                                 int64_t M, int64_t K, int fmt, int mode, void* y,
+                                 int64_t ld_y, int out_dtype, void* stream) {
+  tk_status st = check_dequant_args(M, K, fmt, mode, ld_codes, ld_y, out_dtype);
+  if (st != TK_OK) return st;
+  if (M == 0) return TK_OK;
+  st = check_dequant_pointers(codes, ld_codes, scales, 16, y, ld_y, out_dtype);
+  if (st != TK_OK) return st;
+  return channel_dequant(codes, ld_codes, scales, M, K, fmt, mode, y, ld_y, out_dtype, stream);
 }
 
 }  // extern "C"

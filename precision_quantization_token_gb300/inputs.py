@@ -23,6 +23,7 @@ Workloads are the shapes and value mixes the per-token cast is measured on:
   r2   RMSNorm (eps 1e-6, gain 1 + 0.1 N(0,1)) fused with the per-token cast
        of c2's input: E4M3, group 128, UE8M0 packed
   pc2  per-channel cast (one scale per column) of c2's input, E4M3, fp32
+  pbd2 / pcd2  dequantization of pb2's / pc2's codes and scales to BF16
 
 Random draws use numpy's PCG64 generator seeded per workload; fp32 values are
 rounded to BF16 with round-to-nearest-even on the bit pattern.
@@ -50,6 +51,7 @@ class Workload:
     dist: str
     op: str = "cast"   # "cast" | "swiglu" | "dequant" | "cast_back"
     #                  | "block" | "channel" | "rmsnorm"
+    #                  | "block_dequant" | "channel_dequant"
     eps: float = 1e-6  # RMSNorm
 
     @property
@@ -74,8 +76,8 @@ class Workload:
         if self.op == "cast_back":
             read = self.M * self.K * 2
             return {"read": read, "bf16_out": read, "total": 2 * read}
-        if self.op in ("block", "channel"):
-            if self.op == "block":
+        if self.op in ("block", "channel", "block_dequant", "channel_dequant"):
+            if self.op.startswith("block"):
                 n = -(-self.K // 128)
                 rows = -(-self.M // 128)
             else:
@@ -83,6 +85,9 @@ class Workload:
             words = (n + 3) // 4 if self.scale == "ue8m0" else n
             scales = rows * words * 4
             read = self.M * self.K * 2
+            if self.op.endswith("dequant"):
+                return {"read": codes + scales, "bf16_out": read,
+                        "total": codes + scales + read}
             return {"read": read, "codes": codes, "scales": scales,
                     "total": read + codes + scales}
         read = self.M * self.in_cols * 2
@@ -98,6 +103,10 @@ class Workload:
         if self.op == "channel":
             return (f"per_channel_cast {self.fmt.upper()} {self.scale} "
                     f"{self.M}x{self.K} ({self.dist})")
+        if self.op.endswith("dequant"):
+            kind = "block" if self.op.startswith("block") else "channel"
+            return (f"per_{kind}_dequant {self.fmt.upper()} {self.scale} "
+                    f"{self.M}x{self.K} -> BF16 ({self.dist})")
         op = {"cast": "per_token_cast", "swiglu": "swiglu_per_token_cast",
               "dequant": "per_token_dequant",
               "cast_back": "per_token_cast_back",
@@ -131,6 +140,10 @@ WORKLOADS = {
                     "normal, 0.1% x100 outliers", op="block"),
     "pc2": Workload("pc2", 4096, 7168, 4096, "e4m3", "fp32", "row", False, 2,
                     "normal, 0.1% x100 outliers", op="channel"),
+    "pbd2": Workload("pbd2", 4096, 7168, 128, "e4m3", "fp32", "row", False, 2,
+                     "normal, 0.1% x100 outliers", op="block_dequant"),
+    "pcd2": Workload("pcd2", 4096, 7168, 4096, "e4m3", "fp32", "row", False, 2,
+                     "normal, 0.1% x100 outliers", op="channel_dequant"),
 }
 
 

@@ -272,6 +272,44 @@ def test_rmsnorm_validation(lib, name, kw, want):
     assert call_rms(lib, **kw) == want
 
 
+def call_bd(lib, *, codes=A, ld_codes=256, scales=C, ld_scales=2, M=4,
+            K=256, fmt=0, mode=0, y=B, ld_y=256, out=0):
+    return lib.tk_per_block_dequant(codes, ld_codes, scales, ld_scales, M, K,
+                                    fmt, mode, y, ld_y, out, None)
+
+
+def call_cd(lib, *, codes=A, ld_codes=256, scales=C, M=4, K=256, fmt=0,
+            mode=0, y=B, ld_y=256, out=0):
+    return lib.tk_per_channel_dequant(codes, ld_codes, scales, M, K, fmt, mode,
+                                      y, ld_y, out, None)
+
+
+TILE_DQ_CASES = [
+    ("block bad out dtype", call_bd, dict(out=2), INVALID),
+    ("block K not multiple of 16", call_bd, dict(K=200), INVALID),
+    ("block scale row too narrow", call_bd, dict(ld_scales=1), INVALID),
+    ("block ld_y < K", call_bd, dict(ld_y=128), INVALID),
+    ("block codes misaligned", call_bd, dict(codes=A + 8), MISALIGNED),
+    ("block scales misaligned", call_bd, dict(scales=C + 2), MISALIGNED),
+    ("block fp32 ld_y not 16 bytes", call_bd, dict(K=128, ld_y=130,
+                                                   ld_scales=1, out=1), MISALIGNED),
+    ("block empty batch", call_bd, dict(M=0, codes=None, scales=None, y=None), OK),
+    ("channel bad fmt", call_cd, dict(fmt=3), INVALID),
+    ("channel ld_codes < K", call_cd, dict(ld_codes=128), INVALID),
+    ("channel null scales", call_cd, dict(scales=None), INVALID),
+    ("channel scales not 16-byte aligned", call_cd, dict(scales=C + 4), MISALIGNED),
+    ("channel y misaligned", call_cd, dict(y=B + 2), MISALIGNED),
+    ("channel M too large", call_cd, dict(M=(1 << 30) + 1), UNSUPPORTED),
+    ("channel empty batch", call_cd, dict(M=0, codes=None, scales=None, y=None), OK),
+]
+
+
+@pytest.mark.parametrize("name,fn,kw,want", TILE_DQ_CASES,
+                         ids=[c[0] for c in TILE_DQ_CASES])
+def test_tile_dequant_validation(lib, name, fn, kw, want):
+    assert fn(lib, **kw) == want
+
+
 def test_per_channel_workspace_size(lib):
     # maxima for K rounded up to 128 channels + one counter per 128 (16-B units)
     assert tk.tk_per_channel_workspace_bytes(256) == 4 * 256 + 16

@@ -259,3 +259,128 @@ def test_tensor_api():
 
 def test_zz_no_tile_kernel_gave_up_on_a_wait():
     assert tk.tk_get_device_fault(clear=False) == 0
+
+
+# ------------------------------------------------- per-block / per-channel
+# dequantization: bit-exact against the oracle on the same host codes and
+# scales (from the oracle's casts, and random codes with every scale byte)
+
+def _run_dequant(kind, codes, scales, M, K, fmt, mode, out, ld_y=None):
+    torch = torch_mod()
+    rb = _row_bytes(K, fmt)
+    ld_codes = codes.shape[1]
+    assert ld_codes % 16 == 0 and ld_codes >= rb
+    ld_y = ld_y or K
+    esz = 4 if out == "fp32" else 2
+    y = np.full((M + 2, ld_y * esz), 0xA5, np.uint8)
+    cd = _dev(np.ascontiguousarray(codes))
+    sd = _dev(np.ascontiguousarray(scales).view(np.uint8))
+    yd = _dev(y)
+    if kind == "block":
+        tk.tk_per_block_dequant(cd.data_ptr(), ld_codes, sd.data_ptr(),
+                                scales.shape[1], M, K, tk.FMT[fmt],
+                                tk.SCALE[mode], yd.data_ptr() + ld_y * esz,
+                                ld_y, tk.OUT_DTYPE[out], _stream())
+    else:
+        tk.tk_per_channel_dequant(cd.data_ptr(), ld_codes, sd.data_ptr(), M,
+                                  K, tk.FMT[fmt], tk.SCALE[mode],
+                                  yd.data_ptr() + ld_y * esz, ld_y,
+                                  tk.OUT_DTYPE[out], _stream())
+    torch.cuda.synchronize()
+    g = yd.cpu().numpy()
+    ref = y.copy()
+    if kind == "block":
+        yo = oracle.per_block_dequant(codes, scales, K, 128, FMT_ID[fmt],
+                                      MODE_ID[mode], out_fp32=out == "fp32",
+                                      threads=THREADS)
+    else:
+        yo = oracle.per_channel_dequant(codes, scales.reshape(-1), K,
+                                        FMT_ID[fmt], MODE_ID[mode],
+                                        out_fp32=out == "fp32", threads=THREADS)
+    ref[1:M + 1, :K * esz] = yo.view(np.uint8).reshape(M, K * esz)
+    return g, ref
+
+
+def _padded_codes(codes, K, fmt):
+    rb = _row_bytes(K, fmt)
+    ld = (rb + 15) // 16 * 16
+    out = np.zeros((codes.shape[0], ld), np.uint8)
+    out[:, :rb] = codes[:, :rb]
+    return out
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("out", ["bf16", "fp32"])
+def test_dequant_of_the_casts(fmt, mode, out):
+    M, K = 1000, 7184
+    bits = bits_with_specials(M, K, seed=41)
+    fid, mid = FMT_ID[fmt], MODE_ID[mode]
+    codes, scales = oracle.per_block_cast(bits, K, 128, fid, mid, threads=THREADS)
+    g, r = _run_dequant("block", _padded_codes(codes, K, fmt), scales, M, K,
+                        fmt, mode, out)
+    assert np.array_equal(g, r)
+    codes, scales = oracle.per_channel_cast(bits, K, fid, mid, threads=THREADS)
+    sv = np.zeros(-(-scales.size // 4) * 4, scales.dtype)  # 16-byte multiple
+    sv[:scales.size] = scales
+    g, r = _run_dequant("channel", _padded_codes(codes, K, fmt), sv, M, K,
+                        fmt, mode, out)
+    assert np.array_equal(g, r)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("mode", ["fp32", "ue8m0"])
+def test_dequant_every_code_and_scale(fmt, mode):
+    """Random code bytes (no NaN codes) under every UE8M0 byte 0..254 (0 is
+    the denormal 2^-127; 255, +inf, makes 0 * inf NaNs whose bit patterns
+    are not defined), or fp32 scales over a wide range."""
+    rng = np.random.default_rng(42)
+    M, K = 256, 1024
+    codes = rng.integers(0, 256, size=(M, _row_bytes(K, fmt)), dtype=np.uint8)
+    if fmt == "e4m3":
+        codes[(codes & 0x7F) == 0x7F] = 0x11
+    codes = _padded_codes(codes, K, fmt)
+    if mode == "ue8m0":
+        blk = rng.integers(0, 255, size=(2, 8), dtype=np.uint8)
+        blk.reshape(-1)[:2] = (0, 254)
+        bs = blk.view(np.int32)
+        ch = (np.arange(K, dtype=np.uint32) % 255).astype(np.uint8)  # 0..254
+        cs = ch.view(np.int32)
+    else:
+        bs = np.exp2(rng.uniform(-40, 40, size=(2, 8))).astype(np.float32)
+        cs = np.exp2(rng.uniform(-40, 40, size=K)).astype(np.float32)
+    for out in ("bf16", "fp32"):
+        g, r = _run_dequant("block", codes, bs, M, K, fmt, mode, out)
+        assert np.array_equal(g, r)
+        g, r = _run_dequant("channel", codes, cs, M, K, fmt, mode, out)
+        assert np.array_equal(g, r)
+
+
+def test_dequant_strided_output_and_tensor_api():
+    torch = torch_mod()
+    M, K = 300, 400
+    bits = bits_with_specials(M, K, seed=43)
+    codes, scales = oracle.per_block_cast(bits, K, 128, oracle.FMT_E4M3,
+                                          oracle.SCALE_FP32)
+    g, r = _run_dequant("block", _padded_codes(codes, K, "e4m3"), scales, M, K,
+                        "e4m3", "fp32", "bf16", ld_y=424)
+    assert np.array_equal(g, r)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    for fmt in FMTS:
+        c, s = tk.per_channel_cast(x, fmt, "ue8m0")
+        y = tk.per_channel_dequant(c, s, K, fmt, "ue8m0", out_dtype="fp32")
+        rc, rs = oracle.per_channel_cast(bits, K, FMT_ID[fmt], oracle.SCALE_UE8M0)
+        yo = oracle.per_channel_dequant(rc, rs, K, FMT_ID[fmt],
+                                        oracle.SCALE_UE8M0, out_fp32=True)
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), yo.view(np.uint32))
+        c, s = tk.per_block_cast(x, fmt, "pow2")
+        y = tk.per_block_dequant(c, s, K, fmt, "pow2")
+        rc, rs = oracle.per_block_cast(bits, K, 128, FMT_ID[fmt],
+                                       oracle.SCALE_FP32_POW2)
+        yo = oracle.per_block_dequant(rc, rs, K, 128, FMT_ID[fmt],
+                                      oracle.SCALE_FP32_POW2)
+        assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), yo)
+
+
+def test_zz_dequant_fault_word_clear():
+    assert tk.tk_get_device_fault(clear=False) == 0
