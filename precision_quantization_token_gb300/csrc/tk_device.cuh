@@ -103,12 +103,6 @@ __device__ __forceinline__ uint2 lds8(uint32_t addr) {
   return v;
 }
 
-// Two BF16 values in one 32-bit word -> two fp32 values (exact widening).
-__device__ __forceinline__ void widen2(uint32_t w, float& lo, float& hi) {
-  lo = __uint_as_float(w << 16);
-  hi = __uint_as_float(w & 0xFFFF0000u);
-}
-
 // BF16 element e (a compile-time index after unrolling) of a loaded chunk.
 template <int N8>
 __device__ __forceinline__ float bf16_at(const uint4 (&r)[N8], int e) {
@@ -116,17 +110,6 @@ __device__ __forceinline__ float bf16_at(const uint4 (&r)[N8], int e) {
   const int w = (e % 8) / 2;
   const uint32_t word = w == 0 ? q.x : w == 1 ? q.y : w == 2 ? q.z : q.w;
   return __uint_as_float((e & 1) ? (word & 0xFFFF0000u) : (word << 16));
-}
-
-template <int N8>
-__device__ __forceinline__ void widen(const uint4 (&raw)[N8], float (&v)[N8 * 8]) {
-#pragma unroll
-  for (int i = 0; i < N8; ++i) {
-    widen2(raw[i].x, v[8 * i + 0], v[8 * i + 1]);
-    widen2(raw[i].y, v[8 * i + 2], v[8 * i + 3]);
-    widen2(raw[i].z, v[8 * i + 4], v[8 * i + 5]);
-    widen2(raw[i].w, v[8 * i + 6], v[8 * i + 7]);
-  }
 }
 
 // ------------------------------------------------------------ conversions
@@ -275,27 +258,6 @@ __device__ __forceinline__ bool pow2_settled(float m) {
   return mant > (1u << 10) && mant < (1u << 23) - (1u << 10);
 }
 
-// x / s rounded to nearest: exact product for a power-of-two scale, else the
-// reciprocal estimate q0 plus one residual correction q0 - (q0*s - x) * inv.
-// The residual is formed as q0*s - x and subtracted (rather than x - q0*s
-// added) so that x = -0 gives -0: every zero term then carries x's sign.  The
-// sequence is written in PTX so that no compiler rewrite (such as folding
-// the negation into the first FMA, which breaks signed zeros) can alter it.
-template <bool POW2>
-__device__ __forceinline__ float quotient(float x, const GroupScale& g) {
-  if constexpr (POW2) return x * g.inv;
-  float q;
-  asm("{\n\t.reg .f32 q0, r, nx;\n\t"
-      "mul.rn.f32 q0, %1, %2;\n\t"
-      "neg.f32 nx, %1;\n\t"
-      "fma.rn.f32 r, q0, %3, nx;\n\t"
-      "neg.f32 r, r;\n\t"
-      "fma.rn.f32 %0, r, %2, q0;\n\t}"
-      : "=f"(q)
-      : "f"(x), "f"(g.inv), "f"(g.s));
-  return q;
-}
-
 // ------------------------------------------------------- packed pairs
 //
 // Two-wide forms of the steps above for BF16 input, using the packed fp32
@@ -331,15 +293,22 @@ __device__ __forceinline__ float bmax_value(uint32_t m) {
 
 // Quotients of the two BF16 values in `w` (element 0 in the low half).
 // Power-of-two scales: the exact products x * 2^-k, with inv2 = (2^-k, 2^-k)
-// or any per-half pair of such powers.  fp32 scales: quotient()'s sequence
-// written on negated operands, with s2 the scales and ninv2 the negated
-// reciprocals RN(1/s) of the two halves:
-//   q0 = RN((-x) * (-inv))        = RN(x * inv), same sign: quotient's q0
-//   r  = RN(q0 * s + (-x))        = quotient's residual before its negation
-//   q  = RN(r * (-inv) + q0)      = quotient's RN((-r) * inv + q0)
+// or any per-half pair of such powers.
+// fp32 scales: x / s rounded to nearest from the correctly rounded
+// reciprocal inv = RN(1/s) and one FMA residual correction (Markstein's
+// method), q0 = RN(x * inv), r = RN(q0 * s - x), q = RN(q0 - r * inv); the
+// residual is formed as q0 * s - x and subtracted so that x = -0 gives -0.
+// The kernels run it on negated operands, with s2 the scales and inv2 the
+// negated reciprocals -inv of the two halves, and -x the BF16 pair with both
+// sign bits flipped, widened:
+//   q0 = RN((-x) * (-inv))        = RN(x * inv), the same sign
+//   r  = RN(q0 * s + (-x))        = RN(q0 * s - x)
+//   q  = RN(r * (-inv) + q0)      = RN(q0 - r * inv)
 // Each line has the same exact operand value and the same sign for every
-// zero term as quotient()'s, so q is bit-identical (signed zeros included);
-// -x is the BF16 pair with both sign bits flipped, widened.
+// zero term, so the negated form is bit-identical, signed zeros included
+// (the host proof enumerates every (x, s) pair the casts produce and checks
+// that this equals the IEEE quotient, or, below 2^-64, the same code).  The
+// sequence is written in PTX so that no compiler rewrite can alter it.
 template <bool POW2>
 __device__ __forceinline__ void quotient2(uint32_t w, uint64_t s2, uint64_t inv2,
                                           float& q_lo, float& q_hi) {
