@@ -111,9 +111,12 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the per-token cast kernel is built from (its
+    translation unit, the shared device header, the public header)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(
-        ROOT, "precision_quantization_token_gb300", "csrc", "*"))) + \
+    csrc = os.path.join(ROOT, "precision_quantization_token_gb300", "csrc")
+    files = [os.path.join(csrc, f) for f in ("tk_cast.cu", "tk_device.cuh",
+                                              "tk_internal.h")] + \
         sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
     for p in files:
         with open(p, "rb") as f:
