@@ -132,5 +132,47 @@ def test_tensor_api():
     assert (gc != rc).mean() <= 1e-3
 
 
+
+def test_beyond_2_31_elements():
+    """More than 2^31 elements: the input repeats a 997-row host block, so
+    row m equals host row m % 997; sampled rows on both sides of 2^31
+    elements must equal the kernel's own result for those host rows (a
+    small launch) exactly, and that result meets the tolerance above."""
+    import oracle
+    torch = torch_mod()
+    K, hb, group = 8192, 997, 128
+    M = (1 << 31) // K + 1000
+    block = random_bf16(126, hb, K, scale=2.0)
+    g = gain(K, 126)
+    small = Case(block, K, group, "e4m3", "ue8m0", "row", gain=g, eps=1e-6)
+    check(small)                                   # the host rows themselves
+    ref_codes, ref_scales = small.run_gpu()
+    dev_block = torch.from_numpy(block.view(np.int16)).cuda()
+    x = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    for r0 in range(0, M, hb):
+        n = min(hb, M - r0)
+        x[r0:r0 + n] = dev_block[:n]
+    wd = torch.from_numpy(g.view(np.int16)).cuda()
+    codes = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    G = K // group
+    scales = torch.empty((M, (G + 3) // 4), dtype=torch.int32, device="cuda")
+    tk.tk_rmsnorm_per_token_cast(x.data_ptr(), wd.data_ptr(), M, K, K, 1e-6,
+                                 group, tk.FMT["e4m3"], tk.SCALE["ue8m0"],
+                                 tk.LAYOUT["row"], codes.data_ptr(), K,
+                                 scales.data_ptr(), scales.shape[1],
+                                 torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    edge = (1 << 31) // K
+    sample = sorted({0, 1, M // 2, edge - 1, edge, edge + 1, M - 2, M - 1})
+    idx = torch.tensor(sample, device="cuda")
+    got_c = codes.index_select(0, idx).cpu().numpy()
+    got_s = scales.index_select(0, idx).cpu().numpy().view(np.uint32)
+    for i, m in enumerate(sample):
+        assert np.array_equal(got_c[i], ref_codes[1 + m % hb, :K]), m
+        assert np.array_equal(got_s[i], ref_scales[1 + m % hb, :(G + 3) // 4]), m
+    del x, codes, scales
+    torch.cuda.empty_cache()
+
+
 def test_zz_no_kernel_gave_up_on_a_wait():
     assert tk.tk_get_device_fault(clear=False) == 0

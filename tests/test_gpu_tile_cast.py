@@ -384,3 +384,87 @@ def test_dequant_strided_output_and_tensor_api():
 
 def test_zz_dequant_fault_word_clear():
     assert tk.tk_get_device_fault(clear=False) == 0
+
+
+# ------------------------------------------------------------ large index
+
+def _tiled_device_matrix(torch, block, M):
+    """A device [M, K] int16 matrix repeating the host block's rows."""
+    K = block.shape[1]
+    dev_block = torch.from_numpy(block.view(np.int16)).cuda()
+    x = torch.empty((M, K), dtype=torch.int16, device="cuda")
+    for r0 in range(0, M, block.shape[0]):
+        n = min(block.shape[0], M - r0)
+        x[r0:r0 + n] = dev_block[:n]
+    return x
+
+
+def test_per_block_beyond_2_31_elements():
+    """More than 2^31 elements (64-bit addressing): the input repeats a
+    1,152-row host block (9 block rows), so block row i equals host block
+    row i mod 9; sampled block rows on both sides of 2^31 elements are
+    checked against the oracle's cast of the host block."""
+    torch = torch_mod()
+    K, hb = 16384, 1152
+    M = -(-((1 << 31) // K + 1000) // 128) * 128
+    block = random_bf16(124, hb, K, scale=3.0)
+    x = _tiled_device_matrix(torch, block, M)
+    n_cb = K // 128
+    codes = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((M // 128, n_cb), dtype=torch.float32, device="cuda")
+    tk.tk_per_block_cast(x.data_ptr(), M, K, K, 0, 0, codes.data_ptr(), K,
+                         scales.data_ptr(), n_cb, _stream())
+    torch.cuda.synchronize()
+    rc, rs = oracle.per_block_cast(block, K, 128, oracle.FMT_E4M3,
+                                   oracle.SCALE_FP32, threads=THREADS)
+    edge = (1 << 31) // K // 128                       # block row at 2^31
+    for bi in sorted({0, 1, edge - 1, edge, edge + 1, M // 128 - 1}):
+        lo = (bi % (hb // 128)) * 128
+        got = codes[bi * 128:(bi + 1) * 128].cpu().numpy()
+        assert np.array_equal(got, rc[lo:lo + 128]), bi
+        assert np.array_equal(scales[bi].cpu().numpy().view(np.uint32),
+                              rs[bi % (hb // 128)].view(np.uint32)), bi
+    del x, codes, scales
+    torch.cuda.empty_cache()
+
+
+def test_per_channel_beyond_2_31_elements():
+    """More than 2^31 elements: the input repeats a 999-row host block, and
+    the last row (past 2^31 elements) holds outliers in some columns, so
+    every column maximum and hence every scale depends on rows the 32-bit
+    offsets could not reach."""
+    torch = torch_mod()
+    K, hb = 16384, 999
+    M = (1 << 31) // K + 1000
+    block = random_bf16(125, hb, K)
+    x = _tiled_device_matrix(torch, block, M)
+    last = np.zeros((1, K), np.uint16)
+    last[0, ::7] = 0x4480                                  # 1024, a new column max
+    x[M - 1] = torch.from_numpy(last.view(np.int16)).cuda()[0]
+    codes = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(K, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(tk.tk_per_channel_workspace_bytes(K), dtype=torch.uint8,
+                     device="cuda")
+    tk.tk_per_channel_cast(x.data_ptr(), M, K, K, 0, 0, codes.data_ptr(), K,
+                           scales.data_ptr(), ws.data_ptr(), ws.numel(),
+                           _stream())
+    torch.cuda.synchronize()
+    host = np.vstack([block, last])
+    rc, rs = oracle.per_channel_cast(host, K, oracle.FMT_E4M3,
+                                     oracle.SCALE_FP32, threads=THREADS)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32),
+                          rs.view(np.uint32))
+    edge = (1 << 31) // K
+    sample = sorted({0, 1, M // 2, edge - 1, edge, edge + 1, M - 2})
+    idx = torch.tensor(sample, device="cuda")
+    got = codes.index_select(0, idx).cpu().numpy()
+    for i, m in enumerate(sample):
+        assert np.array_equal(got[i], rc[m % hb]), m
+    assert np.array_equal(codes[M - 1].cpu().numpy(), rc[hb])
+    assert not ws.cpu().numpy().any()
+    del x, codes, scales
+    torch.cuda.empty_cache()
+
+
+def test_zz_large_index_fault_word_clear():
+    assert tk.tk_get_device_fault(clear=False) == 0
