@@ -456,9 +456,9 @@ struct ChannelDequantParams {
   int y_fp32;
 };
 
-constexpr int kDequantThreads = 64;
-constexpr int kDequantRows = 4;            // rows per thread per step
-constexpr int kDequantCtasPerSm = 32;
+constexpr int kDequantThreads = 32;
+constexpr int kDequantRows = 2;         // rows per thread per step
+constexpr int kDequantCtasPerSm = 64;   // blocks per SM the grid aims at
 
 template <int FMT>
 __global__ void __launch_bounds__(kDequantThreads)

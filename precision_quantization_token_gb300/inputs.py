@@ -85,7 +85,7 @@ class Workload:
             words = (n + 3) // 4 if self.scale == "ue8m0" else n
             scales = rows * words * 4
             read = self.M * self.K * 2
-            if self.op.endswith("dequant"):
+            if self.op in ("block_dequant", "channel_dequant"):
                 return {"read": codes + scales, "bf16_out": read,
                         "total": codes + scales + read}
             return {"read": read, "codes": codes, "scales": scales,
@@ -103,7 +103,7 @@ class Workload:
         if self.op == "channel":
             return (f"per_channel_cast {self.fmt.upper()} {self.scale} "
                     f"{self.M}x{self.K} ({self.dist})")
-        if self.op.endswith("dequant"):
+        if self.op in ("block_dequant", "channel_dequant"):
             kind = "block" if self.op.startswith("block") else "channel"
             return (f"per_{kind}_dequant {self.fmt.upper()} {self.scale} "
                     f"{self.M}x{self.K} -> BF16 ({self.dist})")
