@@ -227,16 +227,28 @@ struct GroupScale {
 template <int FMT, bool POW2>
 __device__ __forceinline__ GroupScale group_scale(float amax) {
   constexpr float kMax = FMT == TK_FMT_E4M3 ? 448.0f : 6.0f;
-  const float r = __fdiv_rn(fmaxf(amax, 1e-4f), kMax);
+  const float a = fmaxf(amax, 1e-4f);
   GroupScale g;
   if constexpr (POW2) {
-    // r is a positive normal number (>= 1e-4/448); 2^ceil(log2 r) keeps its
-    // exponent when the mantissa is zero and bumps it otherwise.
-    const uint32_t u = __float_as_uint(r);
-    g.e = (u >> 23) + ((u & 0x7FFFFFu) != 0u);
+    // 2^ceil(log2 RN(a / fmt_max)) without the division.  With
+    // a = m * 2^(E-127), m in [1, 2), and fmt_max = 1.75 * 2^8 (E4M3) or
+    // 1.5 * 2^2 (E2M1), the exact ratio is (m / 1.75) * 2^(E-135) or
+    // (m / 1.5) * 2^(E-129): at most that power of two while m is at most
+    // 1.75 (1.5), just above it otherwise, so the biased exponent is E - 8
+    // (E - 2) plus one when a's mantissa field exceeds 1.75's (1.5's).
+    // Rounding the ratio to fp32 first changes nothing: a ratio above a
+    // power of two is more than half an ulp above it (m exceeds 1.75 by a
+    // whole ulp of a, over 4/7 of an ulp of the ratio; 2/3 for 1.5).  a is
+    // at least 1e-4 and finite, so the exponent lies in [105, 253] and
+    // 2^-k is normal.
+    constexpr uint32_t kDrop = FMT == TK_FMT_E4M3 ? 8u : 2u;
+    constexpr uint32_t kMant = FMT == TK_FMT_E4M3 ? 0x600000u : 0x400000u;
+    const uint32_t u = __float_as_uint(a);
+    g.e = (u >> 23) - kDrop + ((u & 0x7FFFFFu) > kMant);
     g.s = __uint_as_float(g.e << 23);
-    g.inv = __uint_as_float((254u - g.e) << 23);   // e <= 253, so 2^-k is normal
+    g.inv = __uint_as_float((254u - g.e) << 23);
   } else {
+    const float r = __fdiv_rn(a, kMax);
     g.s = r;
     g.inv = __frcp_rn(r);
     g.e = 0;

@@ -10,6 +10,11 @@ GPU (no flush to zero on either side), so the host enumeration proves the
 device arithmetic.  The CUDA source is checked to still use that sequence
 (the packed negated-operand form, in every kernel that divides by an fp32
 scale).
+
+The power-of-two scales' exponent is taken from the bits of the floored
+amax instead of dividing; that rule is checked against the definition
+(exponent of RN(max(a, 1e-4) / fmt_max), rounded up to a power of two) for
+every positive finite fp32 amax of both formats.
 """
 import os
 import platform
@@ -21,6 +26,7 @@ import pytest
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "quotient_check.c")
+EXP_SRC = os.path.join(HERE, "pow2_exponent_check.c")
 CU = os.path.join(ROOT, "precision_quantization_token_gb300", "csrc",
                   "tk_device.cuh")
 
@@ -107,3 +113,47 @@ def test_every_reachable_pair(results, fmt_max):
     assert form == 0, "the negated-operand form differs from the sequence"
     print(f"{pairs} pairs; {sub} quotients below 2^-64 off by the residual "
           "underflow, all encoding to the same signed zero")
+
+
+@pytest.fixture(scope="module")
+def exponent_results(tmp_path_factory):
+    """The exponent rule over every positive finite fp32 amax, for both
+    formats, and the wrong rule (mantissa field >= the threshold) that the
+    enumeration must reject; four processes at once."""
+    exe = str(tmp_path_factory.mktemp("e") / "pow2_exponent_check")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off",
+                    "-fno-fast-math", "-o", exe, EXP_SRC], check=True)
+    runs = {(f, m): subprocess.Popen([exe, f, *([m] if m else [])],
+                                     stdout=subprocess.PIPE,
+                                     stderr=subprocess.PIPE, text=True)
+            for f in ("448", "6") for m in ("", "ge")}
+    out = {}
+    for key, p in runs.items():
+        stdout, stderr = p.communicate(timeout=900)
+        assert p.returncode == 0, stderr
+        out[key] = tuple(map(int, stdout.split())) + (stderr,)
+    return out
+
+
+def test_kernels_take_the_exponent_from_the_amax_bits():
+    """group_scale's power-of-two branch: e = E - 8 (E4M3) or E - 2 (E2M1),
+    plus one when the mantissa field exceeds 1.75's (0x600000) or 1.5's
+    (0x400000); the fp32 branch keeps the IEEE division."""
+    src = open(CU).read()
+    body = src[src.index("GroupScale group_scale(float amax) {"):]
+    body = body[:body.index("\n}\n")]
+    assert "kDrop = FMT == TK_FMT_E4M3 ? 8u : 2u;" in body
+    assert "kMant = FMT == TK_FMT_E4M3 ? 0x600000u : 0x400000u;" in body
+    assert "const float a = fmaxf(amax, 1e-4f);" in body
+    assert "g.e = (u >> 23) - kDrop + ((u & 0x7FFFFFu) > kMant);" in body
+    assert "const float r = __fdiv_rn(a, kMax);" in body
+
+
+@pytest.mark.parametrize("fmt_max", ["448", "6"])
+def test_exponent_rule_on_every_amax(exponent_results, fmt_max):
+    values, bad, stderr = exponent_results[(fmt_max, "")]
+    assert values == 0x7F800000          # +0 through the largest finite fp32
+    assert bad == 0, stderr
+    # the enumeration does tell rules apart: >= in place of > must fail
+    wrong_values, wrong_bad, _ = exponent_results[(fmt_max, "ge")]
+    assert wrong_values == values and wrong_bad > 0
