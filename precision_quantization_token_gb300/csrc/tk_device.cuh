@@ -90,6 +90,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
       ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// One BF16 element of shared memory, widened to fp32.
+__device__ __forceinline__ float lds_bf16(uint32_t addr) {
+  uint16_t h;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr));
+  return __uint_as_float((uint32_t)h << 16);
+}
+
 __device__ __forceinline__ uint4 lds16(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -257,17 +264,17 @@ __device__ __forceinline__ GroupScale group_scale(float amax) {
 }
 
 // True when every amax within a relative 2^-16 of m gives the same
-// power-of-two scale.  The scale is 2^ceil(log2(max(a, 1e-4) / fmt_max)),
-// which only changes where that ratio crosses a power of two; with
-// r ~ max(m, 1e-4) / fmt_max (one multiply, relative error below 2^-23), a
-// mantissa field at least 2^10 away from both ends of the binade keeps r
-// more than 2^-13 (relative) from every power of two, so no perturbation
-// of 2^-16 (nor the rounding of the division) can cross one.
+// power-of-two scale.  By the exponent rule of group_scale the scale only
+// changes where the floored amax crosses 1.75 * 2^j (E4M3) or 1.5 * 2^j
+// (E2M1), i.e. where its mantissa field passes 0x600000 (0x400000); moving
+// by a relative 2^-16 shifts that field by less than 2^8, so a field more
+// than 2^8 from the threshold cannot cross it (nor any other crossing
+// point, which lies a whole binade or more away).
 template <int FMT>
 __device__ __forceinline__ bool pow2_settled(float m) {
-  constexpr float kInvMax = FMT == TK_FMT_E4M3 ? 1.0f / 448.0f : 1.0f / 6.0f;
-  const uint32_t mant = __float_as_uint(fmaxf(m, 1e-4f) * kInvMax) & 0x7FFFFFu;
-  return mant > (1u << 10) && mant < (1u << 23) - (1u << 10);
+  constexpr uint32_t kMant = FMT == TK_FMT_E4M3 ? 0x600000u : 0x400000u;
+  const uint32_t f = __float_as_uint(fmaxf(m, 1e-4f)) & 0x7FFFFFu;
+  return f - kMant + 256u > 512u;           // |f - kMant| > 256 (unsigned wrap)
 }
 
 // ------------------------------------------------------- packed pairs
@@ -379,6 +386,32 @@ __device__ __forceinline__ float max_abs2(float c, float a, float b) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(c), "f"(fabsf(a)), "f"(fabsf(b)));
   return d;
+}
+
+// Exact products of two BF16 pairs, (a.lo * b.lo, a.hi * b.hi), as an fp32
+// pair, straight from the packed halves (mixed-precision fma, sm_100 and
+// later).  A product of two BF16 values has at most 16 significant bits, so
+// it is exact in fp32 unless it falls below 2^-126; adding -0 keeps every
+// value (signed zeros too), and the one rounding is that of the fp32
+// multiply of the widened values.
+__device__ __forceinline__ uint64_t bmul2(uint32_t a, uint32_t b) {
+  uint64_t d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t.reg .f32 lo, hi;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 lo, al, bl, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 hi, ah, bh, 0f80000000;\n\t"
+      "mov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Sums of squares of a BF16 pair: s0 = RN(a.lo^2 + s0), s1 = RN(a.hi^2 + s1),
+// the same single roundings as an fp32 FMA on the widened values.
+__device__ __forceinline__ void bsq_acc2(uint32_t a, float& s0, float& s1) {
+  asm("{\n\t.reg .b16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, al, %0;\n\t"
+      "fma.rn.f32.bf16 %1, ah, ah, %1;\n\t}"
+      : "+f"(s0), "+f"(s1) : "r"(a));
 }
 
 // quotient2's reciprocal operand for a scale: 2^-k for power-of-two

@@ -240,6 +240,74 @@ def test_swiglu_fp32_scales_track_the_exact_product():
     assert np.count_nonzero(sg != sr) <= 2, np.count_nonzero(sg != sr)
 
 
+def _near_edge_pairs(fmt_max, rng):
+    """BF16 (gate, up) bit pairs whose SwiGLU value lies within a relative
+    2^-13 of +-fmt_max * 2^j, where the power-of-two scale changes, and the
+    relative offset of each.  Found by enumerating BF16 gates in [-6, 10]
+    and ups of every mantissa over 22 binades with the plain double
+    formula; this only chooses inputs (the expected values are the
+    oracle's)."""
+    g = np.arange(0, 0x10000, dtype=np.uint32)
+    g = g[((g >> 7) & 0xFF) != 0xFF]                 # finite patterns only
+    gv = bf16_bits_to_f32(g.astype(np.uint16)).astype(np.float64)
+    gsel = g[(gv >= -6) & (gv <= 10) & (np.abs(gv) > 0.05)]
+    ub = np.array([(e << 7) | m for e in range(114, 136) for m in range(128)],
+                  np.uint32)
+    gq = bf16_bits_to_f32(gsel.astype(np.uint16)).astype(np.float64)
+    uq = bf16_bits_to_f32(ub.astype(np.uint16)).astype(np.float64)
+    y = np.abs(gq[:, None] * uq[None, :] / (1.0 + np.exp(-gq[:, None])))
+    t = np.log2(y / fmt_max)
+    rel = (t - np.round(t)) * np.log(2.0)        # relative offset from the edge
+    gi, ui = np.nonzero((np.abs(rel) <= 2.0 ** -13) & (y >= 1e-2))
+    sign = rng.integers(0, 2, gi.size).astype(np.uint32) << 15
+    return gsel[gi], ub[ui] | sign, rel[gi, ui]
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("mode", ["pow2", "ue8m0"])
+def test_swiglu_pow2_scales_at_the_switching_points(fmt, mode):
+    """Power-of-two scales where they change: every group's amax element
+    sits within a relative 2^-13 of fmt_max * 2^j, about half of them
+    inside the +-2^-15 band that the kernel re-evaluates exactly and the
+    rest on the side it settles from the fp32 amax alone.  The scale bytes
+    must equal the oracle's exactly (no edge allowance)."""
+    fmt_max = 448.0 if fmt == "e4m3" else 6.0
+    rng = np.random.default_rng(31)
+    pg, pu, rel = _near_edge_pairs(fmt_max, rng)
+    inner = np.abs(rel) <= 2.0 ** -15
+    assert inner.sum() >= 200 and (~inner).sum() >= 200
+    M, N, group = 64, 2048, 128
+    G = N // group
+    pick = rng.integers(0, pg.size, M * G)
+    assert inner[pick].sum() >= 100 and (~inner[pick]).sum() >= 100
+    gate = np.clip(rng.standard_normal((M, N)), -3, 3).astype(np.float32)
+    up = rng.uniform(-1, 1, (M, N)).astype(np.float32)
+    gate_b = f32_to_bf16_bits(gate)
+    up_b = f32_to_bf16_bits(up)
+    ga = bf16_bits_to_f32(pg[pick].astype(np.uint16))
+    ua = bf16_bits_to_f32(pu[pick].astype(np.uint16))
+    y_edge = np.abs(ga.astype(np.float64) * ua / (1.0 + np.exp(-ga.astype(np.float64))))
+    planted = np.empty((M, G), np.int64)
+    for k in range(M * G):
+        m, j = divmod(k, G)
+        cols = slice(j * group, (j + 1) * group)
+        # the others stay below 0.3 of the edge element: |silu(g)| <= 3
+        up_b[m, cols] = f32_to_bf16_bits(up[m, cols] * np.float32(0.1 * y_edge[k]))
+        at = j * group + int(rng.integers(0, group))
+        gate_b[m, at] = pg[pick[k]]
+        up_b[m, at] = pu[pick[k]]
+        planted[m, j] = at
+    bits = np.concatenate([gate_b, up_b], axis=1)
+    # the planted element is its group's amax in the oracle's values
+    y = np.abs(oracle.swiglu_values(bits, N, threads=THREADS)).reshape(M, G, group)
+    assert np.array_equal(y.argmax(axis=2) + np.arange(G) * group, planted)
+    case = Case(bits, N, group, fmt, mode, "row", swiglu=True)
+    gc, gs = case.run_gpu()
+    rc, rs = case.run_oracle()
+    assert np.array_equal(gs, rs), np.count_nonzero(gs != rs)
+    check_swiglu(case, gpu=(gc, gs), ref=(rc, rs), max_code_frac=2e-3)
+
+
 def test_swiglu_zero_gate_and_strided():
     M, N, group = 33, 256, 64
     bits = random_bf16(8, M, 2 * N)

@@ -94,7 +94,15 @@ def test_fp32_input_paths_use_the_negated_form():
     assert "const uint64_t ni = pack_f32x2(-gs.inv, -gs.inv);" in sw
     assert "const uint64_t q0 = fmul2(ny[i], ni);" in sw
     assert "r = ffma2(ffma2(q0, s2, ny[i]), ni, q0);" in sw
-    assert "ny[i] = pack_f32x2(-v0, -v1);" in sw              # slow path
+    # both SwiGLU paths form -y directly: the packed fast path with the
+    # denominator negated, RN(t * -1 + -1), the per-element path through
+    # swiglu_neg (the same scalar sequence, or -(the IEEE fallback))
+    assert "const uint64_t d = ffma2(pack_f32x2(t0, t1), m1, m1);" in sw
+    assert "ny[i] = pack_f32x2(swiglu_neg(" in sw
+    neg = src[src.index("float swiglu_fast_neg(float gate, float up) {"):]
+    neg = neg[:neg.index("\n}\n")]
+    assert '"f"(-1.0f - t)' in neg and "return (gate * up) * r;" in neg
+    assert ": -swiglu_ieee(gate, up);" in src
     rms = src[src.index("__device__ __forceinline__ void rms_chunk("):]
     rms = rms[:rms.index("\n}\n")]
     assert "const float f = POW2 ? rstd : -rstd;" in rms      # -y for fp32 scales
