@@ -21,7 +21,8 @@
  *
  * Conventions shared by every entry point:
  *  - All data pointers are DEVICE pointers (global memory of the current
- *    CUDA device).  The caller allocates and owns every buffer; the library
+ *    CUDA device), except the x, codes and scales of the two *_host entry
+ *    points.  The caller allocates and owns every buffer; the library
  *    allocates nothing and keeps no pointer after the call returns.
  *  - Calls are asynchronous: they validate on the host, enqueue their work
  *    on `stream` (a cudaStream_t passed as void*, NULL = legacy default
@@ -134,6 +135,59 @@ TK_API tk_status tk_swiglu_per_token_cast(const void *x, int64_t M, int64_t N,
                                    int layout, void *codes, int64_t ld_codes,
                                    void *scales, int64_t ld_scales,
                                    void *stream);
+
+/*
+ * Host-buffer forms of tk_per_token_cast and tk_swiglu_per_token_cast: the
+ * same operation on rows that live in HOST memory, with codes and scales
+ * delivered to host memory.  These are the only entry points that take
+ * host pointers and the only ones that block: they return once the
+ * outputs are in host memory (or after a failure, once everything they
+ * enqueued has finished).
+ *
+ *   x, codes, scales   HOST buffers with the layouts, strides and
+ *             arguments of tk_per_token_cast (tk_swiglu_per_token_cast: x
+ *             holds [gate | up], K = N).  No alignment rule applies to
+ *             them; page-locked (pinned) memory lets the copies run
+ *             asynchronously and overlap.  Scale entries outside the
+ *             written region and code bytes past each row's K (K/2) bytes
+ *             are left untouched, as on the device.
+ *   scratch   DEVICE memory of at least tk_host_scratch_bytes(...) bytes
+ *             (same M, K, group, fmt, mode, layout; swiglu 1 for the SwiGLU
+ *             form), 16-byte aligned, owned by the caller and not in use by
+ *             pending work on either stream; nothing is read from it.
+ *   chunk_rows   rows per chunk (rounded down to a multiple of 4, at least
+ *             4); 0 picks about 8 MiB of input per chunk.
+ *   stream0, stream1   cudaStream_t as void*; chunks alternate between
+ *             them.  Each chunk's upload, cast and download run in order on
+ *             its stream, so one chunk's upload overlaps the previous
+ *             chunk's cast and download.  They may be the same stream (the
+ *             chunks then run one after another).
+ *   Errors as for tk_per_token_cast, plus TK_ERR_INVALID_ARG for a scratch
+ *   smaller than required or chunk_rows < 0, TK_ERR_MISALIGNED for an
+ *   unaligned scratch, and TK_ERR_CUDA for a failed copy or wait.
+ */
+TK_API size_t tk_host_scratch_bytes(int64_t M, int64_t K, int group, int fmt,
+                                    int mode, int layout, int swiglu);
+
+TK_API tk_status tk_per_token_cast_host(const void *x, int64_t M, int64_t K,
+                                        int64_t ld_x, int group, int fmt,
+                                        int mode, int layout, void *codes,
+                                        int64_t ld_codes, void *scales,
+                                        int64_t ld_scales, void *scratch,
+                                        size_t scratch_bytes,
+                                        int64_t chunk_rows, void *stream0,
+                                        void *stream1);
+
+TK_API tk_status tk_swiglu_per_token_cast_host(const void *x, int64_t M,
+                                               int64_t N, int64_t ld_x,
+                                               int group, int fmt, int mode,
+                                               int layout, void *codes,
+                                               int64_t ld_codes, void *scales,
+                                               int64_t ld_scales,
+                                               void *scratch,
+                                               size_t scratch_bytes,
+                                               int64_t chunk_rows,
+                                               void *stream0, void *stream1);
 
 /*
  * tk_per_token_dequant -- per-token dequantization (TileKernels README,

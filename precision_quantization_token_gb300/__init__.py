@@ -130,6 +130,15 @@ def load():
             lib.tk_per_channel_dequant.restype = i
             lib.tk_per_channel_workspace_bytes.argtypes = [i64]
             lib.tk_per_channel_workspace_bytes.restype = ctypes.c_size_t
+            lib.tk_host_scratch_bytes.argtypes = [i64, i64, i, i, i, i, i]
+            lib.tk_host_scratch_bytes.restype = ctypes.c_size_t
+            hsig = [p, i64, i64, i64, i, i, i, i, p, i64, p, i64, p,
+                    ctypes.c_size_t, i64, p, p]
+            for name in ("tk_per_token_cast_host",
+                         "tk_swiglu_per_token_cast_host"):
+                fn = getattr(lib, name)
+                fn.argtypes = hsig
+                fn.restype = i
             lib.tk_get_device_fault.argtypes = [p, i]
             lib.tk_get_device_fault.restype = i
             lib.tk_status_string.argtypes = [i]
@@ -239,6 +248,36 @@ def tk_per_channel_workspace_bytes(K: int) -> int:
     return int(load().tk_per_channel_workspace_bytes(K))
 
 
+def tk_host_scratch_bytes(M, K, group, fmt, mode, layout, swiglu=0) -> int:
+    """Device scratch bytes of the host-buffer casts (0: bad arguments)."""
+    return int(load().tk_host_scratch_bytes(M, K, group, fmt, mode, layout,
+                                            swiglu))
+
+
+def tk_per_token_cast_host(x_ptr, M, K, ld_x, group, fmt, mode, layout,
+                           codes_ptr, ld_codes, scales_ptr, ld_scales,
+                           scratch_ptr, scratch_bytes, chunk_rows=0,
+                           stream0=0, stream1=0) -> None:
+    """Raw-pointer call of the host-buffer cast (host x, codes, scales;
+    device scratch); blocks until the outputs are in host memory."""
+    _check(load().tk_per_token_cast_host(x_ptr, M, K, ld_x, group, fmt, mode,
+                                         layout, codes_ptr, ld_codes,
+                                         scales_ptr, ld_scales, scratch_ptr,
+                                         scratch_bytes, chunk_rows, stream0,
+                                         stream1))
+
+
+def tk_swiglu_per_token_cast_host(x_ptr, M, N, ld_x, group, fmt, mode, layout,
+                                  codes_ptr, ld_codes, scales_ptr, ld_scales,
+                                  scratch_ptr, scratch_bytes, chunk_rows=0,
+                                  stream0=0, stream1=0) -> None:
+    """Raw-pointer call of the host-buffer fused SwiGLU cast."""
+    _check(load().tk_swiglu_per_token_cast_host(
+        x_ptr, M, N, ld_x, group, fmt, mode, layout, codes_ptr, ld_codes,
+        scales_ptr, ld_scales, scratch_ptr, scratch_bytes, chunk_rows,
+        stream0, stream1))
+
+
 def tk_get_device_fault(clear: bool = False) -> int:
     """The device fault word of the current device (0: no kernel gave up on
     a wait); see include/tk_cast.h."""
@@ -282,33 +321,64 @@ def _outputs(torch, M, K, group, fmt, scale, layout, device, codes, scales):
     return codes, scales
 
 
+_host_streams = {}
+
+
+def _copy_streams(torch, device):
+    """Two streams per device for the host-buffer pipeline (created once)."""
+    key = torch.device(device).index
+    if key not in _host_streams:
+        _host_streams[key] = (torch.cuda.Stream(device), torch.cuda.Stream(device))
+    return _host_streams[key]
+
+
 def _call(entry, x, K, group, fmt, scale, layout, codes, scales, stream):
     import torch
     if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x must be a 2-D bfloat16 tensor with unit column "
                          "stride")
-    on_host = x.device.type == "cpu"
-    xd = x.to("cuda", non_blocking=True) if on_host else x
-    M = xd.shape[0]
-    dev_codes, dev_scales = _outputs(torch, M, K, group, fmt, scale, layout,
-                                     xd.device, None if on_host else codes,
-                                     None if on_host else scales)
+    if x.device.type == "cpu":
+        return _call_host(entry, torch, x, K, group, fmt, scale, layout,
+                          codes, scales)
+    M = x.shape[0]
+    codes, scales = _outputs(torch, M, K, group, fmt, scale, layout, x.device,
+                             codes, scales)
     if stream is None:
-        stream = torch.cuda.current_stream(xd.device).cuda_stream
-    entry(xd.data_ptr(), M, K, xd.stride(0), group, FMT[fmt], SCALE[scale],
-          LAYOUT[layout], dev_codes.data_ptr(), dev_codes.stride(0),
-          dev_scales.data_ptr(), dev_scales.stride(0), stream)
-    if not on_host:
-        return dev_codes, dev_scales
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    entry(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt], SCALE[scale],
+          LAYOUT[layout], codes.data_ptr(), codes.stride(0),
+          scales.data_ptr(), scales.stride(0), stream)
+    return codes, scales
+
+
+def _call_host(entry, torch, x, K, group, fmt, scale, layout, codes, scales):
+    """CPU tensors: the library's host-buffer pipeline (chunks of rows
+    uploaded, cast and downloaded on two streams) on the current device."""
+    M = x.shape[0]
+    swiglu = entry is tk_swiglu_per_token_cast
     if codes is None:
-        codes = torch.empty(dev_codes.shape, dtype=dev_codes.dtype,
-                            pin_memory=True)
+        row_bytes = K if fmt == "e4m3" else K // 2
+        codes = torch.empty((M, row_bytes), dtype=torch.uint8, pin_memory=True)
     if scales is None:
-        scales = torch.empty(dev_scales.shape, dtype=dev_scales.dtype,
-                             pin_memory=True)
-    codes.copy_(dev_codes, non_blocking=True)
-    scales.copy_(dev_scales, non_blocking=True)
-    torch.cuda.current_stream(xd.device).synchronize()
+        shape, dt = scale_shape(M, K, group, scale, layout)
+        scales = torch.empty(shape, dtype=getattr(torch, dt), pin_memory=True)
+    if codes.device.type != "cpu" or scales.device.type != "cpu":
+        raise ValueError("a CPU input takes CPU codes and scales")
+    device = torch.device("cuda", torch.cuda.current_device())
+    need = tk_host_scratch_bytes(M, K, group, FMT[fmt], SCALE[scale],
+                                 LAYOUT[layout], int(swiglu))
+    scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    s0, s1 = _copy_streams(torch, device)
+    # the scratch comes from the current stream's pool: start after it
+    cur = torch.cuda.current_stream(device)
+    s0.wait_stream(cur)
+    s1.wait_stream(cur)
+    host_entry = (tk_swiglu_per_token_cast_host if swiglu
+                  else tk_per_token_cast_host)
+    host_entry(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt], SCALE[scale],
+               LAYOUT[layout], codes.data_ptr(), codes.stride(0),
+               scales.data_ptr(), scales.stride(0), scratch.data_ptr(), need,
+               0, s0.cuda_stream, s1.cuda_stream)
     return codes, scales
 
 
@@ -318,9 +388,10 @@ def per_token_cast(x, group: int = 128, fmt: str = "e4m3",
     """Per-token group-wise cast of a bfloat16 [M, K] tensor.
 
     CUDA input: outputs are CUDA tensors, the call is asynchronous on the
-    current stream.  CPU input (preferably pinned): the input is copied to
-    the current CUDA device, cast there, and the outputs are copied back into
-    (pinned) host tensors before returning.
+    current stream.  CPU input (preferably pinned): the library's host-buffer
+    pipeline uploads the rows in chunks to the current CUDA device, casts
+    them there and downloads codes and scales into (pinned) host tensors,
+    chunks alternating over two streams; returns once they are on the host.
     Returns (codes uint8 [M, K or K/2], scales) -- see ``scale_shape``.
     """
     K = x.shape[1]

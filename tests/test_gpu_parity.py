@@ -384,6 +384,54 @@ def test_host_buffers_match_device_path(fmt, scale, layout, K, group):
                           ds.cpu().numpy().view(np.uint32)[..., :n])
 
 
+@pytest.mark.parametrize("layout", ["row", "transposed"])
+@pytest.mark.parametrize("chunk_rows", [4, 37, 0])
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_host_entry_chunks_and_strides(layout, chunk_rows, swiglu):
+    """The raw host-buffer entry: small and ragged chunks (37 rounds down to
+    36), host row strides wider than the rows and not multiples of 16 (the
+    input pad poisoned, the output pads filled with a sentinel that must
+    survive), pageable numpy memory, and one stream for both chunk streams.
+    Results equal the device-tensor call's bit for bit."""
+    import torch
+    M, K, group, fmt, mode = 203, 384, 64, "e4m3", "fp32"
+    in_cols = 2 * K if swiglu else K
+    bits = random_bf16(41 + swiglu, M, in_cols, scale=3.0)
+    ld_x = in_cols + 40
+    xh = np.full((M, ld_x), 0x7FC0, np.uint16)            # NaN in the pad
+    xh[:, :in_cols] = bits
+    G = K // group
+    ld_codes = K + 24
+    codes = np.full((M, ld_codes), 0xA5, np.uint8)
+    if layout == "row":
+        ld_scales, scale_rows = G + 3, M
+    else:
+        ld_scales, scale_rows = M + 5, G
+    scales = np.full((scale_rows, ld_scales), 0x7F7F7F7F, np.uint32)
+    need = tk.tk_host_scratch_bytes(M, K, group, tk.FMT[fmt], tk.SCALE[mode],
+                                    tk.LAYOUT[layout], int(swiglu))
+    scratch = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    entry = (tk.tk_swiglu_per_token_cast_host if swiglu
+             else tk.tk_per_token_cast_host)
+    entry(xh.ctypes.data, M, K, ld_x, group, tk.FMT[fmt], tk.SCALE[mode],
+          tk.LAYOUT[layout], codes.ctypes.data, ld_codes, scales.ctypes.data,
+          ld_scales, scratch.data_ptr(), need, chunk_rows, s, s)
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    fn = tk.swiglu_per_token_cast if swiglu else tk.per_token_cast
+    dc, ds = fn(x, group=group, fmt=fmt, scale=mode, layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(codes[:, :K], dc.cpu().numpy())
+    assert (codes[:, K:] == 0xA5).all()
+    want = ds.cpu().numpy().view(np.uint32)
+    if layout == "row":
+        assert np.array_equal(scales[:, :G], want[:, :G])
+        assert (scales[:, G:] == 0x7F7F7F7F).all()
+    else:
+        assert np.array_equal(scales[:, :M], want[:, :M])
+        assert (scales[:, M:] == 0x7F7F7F7F).all()
+
+
 def test_bf16_input_values_roundtrip():
     """Sanity: the decoded codes times the scales approximate the input."""
     import torch
