@@ -156,15 +156,20 @@ TK_API tk_status tk_swiglu_per_token_cast(const void *x, int64_t M, int64_t N,
  *             form), 16-byte aligned, owned by the caller and not in use by
  *             pending work on either stream; nothing is read from it.
  *   chunk_rows   rows per chunk (rounded down to a multiple of 4, at least
- *             4); 0 picks about 8 MiB of input per chunk.
- *   stream0, stream1   cudaStream_t as void*; chunks alternate between
- *             them.  Each chunk's upload, cast and download run in order on
- *             its stream, so one chunk's upload overlaps the previous
- *             chunk's cast and download.  They may be the same stream (the
- *             chunks then run one after another).
+ *             4); 0 splits M into about 4 chunks of at least 4 MiB of input
+ *             each (rounded up to a multiple of 4 rows).
+ *   streams, n_streams   an array of 1 to 64 cudaStream_t (as void*; NULL
+ *             entries mean the legacy default stream); chunk i goes to
+ *             streams[i % n_streams].  Each chunk's upload, cast and download
+ *             run in order on its stream, so uploads overlap earlier chunks'
+ *             casts and downloads; an upload waits only for the download of
+ *             the chunk n_streams places earlier, so 3 or 4 distinct streams
+ *             keep the upload engine busy.  Entries may repeat (one stream:
+ *             the chunks run one after another).
  *   Errors as for tk_per_token_cast, plus TK_ERR_INVALID_ARG for a scratch
- *   smaller than required or chunk_rows < 0, TK_ERR_MISALIGNED for an
- *   unaligned scratch, and TK_ERR_CUDA for a failed copy or wait.
+ *   smaller than required, chunk_rows < 0, or a bad stream array,
+ *   TK_ERR_MISALIGNED for an unaligned scratch, and TK_ERR_CUDA for a
+ *   failed copy or wait.
  */
 TK_API size_t tk_host_scratch_bytes(int64_t M, int64_t K, int group, int fmt,
                                     int mode, int layout, int swiglu);
@@ -175,8 +180,8 @@ TK_API tk_status tk_per_token_cast_host(const void *x, int64_t M, int64_t K,
                                         int64_t ld_codes, void *scales,
                                         int64_t ld_scales, void *scratch,
                                         size_t scratch_bytes,
-                                        int64_t chunk_rows, void *stream0,
-                                        void *stream1);
+                                        int64_t chunk_rows,
+                                        void *const *streams, int n_streams);
 
 TK_API tk_status tk_swiglu_per_token_cast_host(const void *x, int64_t M,
                                                int64_t N, int64_t ld_x,
@@ -187,7 +192,8 @@ TK_API tk_status tk_swiglu_per_token_cast_host(const void *x, int64_t M,
                                                void *scratch,
                                                size_t scratch_bytes,
                                                int64_t chunk_rows,
-                                               void *stream0, void *stream1);
+                                               void *const *streams,
+                                               int n_streams);
 
 /*
  * tk_per_token_dequant -- per-token dequantization (TileKernels README,

@@ -133,7 +133,7 @@ def load():
             lib.tk_host_scratch_bytes.argtypes = [i64, i64, i, i, i, i, i]
             lib.tk_host_scratch_bytes.restype = ctypes.c_size_t
             hsig = [p, i64, i64, i64, i, i, i, i, p, i64, p, i64, p,
-                    ctypes.c_size_t, i64, p, p]
+                    ctypes.c_size_t, i64, ctypes.POINTER(p), i]
             for name in ("tk_per_token_cast_host",
                          "tk_swiglu_per_token_cast_host"):
                 fn = getattr(lib, name)
@@ -254,28 +254,35 @@ def tk_host_scratch_bytes(M, K, group, fmt, mode, layout, swiglu=0) -> int:
                                             swiglu))
 
 
+def _stream_array(streams):
+    arr = (ctypes.c_void_p * len(streams))(*[s or None for s in streams])
+    return arr, len(streams)
+
+
 def tk_per_token_cast_host(x_ptr, M, K, ld_x, group, fmt, mode, layout,
                            codes_ptr, ld_codes, scales_ptr, ld_scales,
                            scratch_ptr, scratch_bytes, chunk_rows=0,
-                           stream0=0, stream1=0) -> None:
+                           streams=(0,)) -> None:
     """Raw-pointer call of the host-buffer cast (host x, codes, scales;
-    device scratch); blocks until the outputs are in host memory."""
+    device scratch; chunks dealt over the cudaStream_t handles in
+    `streams`); blocks until the outputs are in host memory."""
+    arr, n = _stream_array(streams)
     _check(load().tk_per_token_cast_host(x_ptr, M, K, ld_x, group, fmt, mode,
                                          layout, codes_ptr, ld_codes,
                                          scales_ptr, ld_scales, scratch_ptr,
-                                         scratch_bytes, chunk_rows, stream0,
-                                         stream1))
+                                         scratch_bytes, chunk_rows, arr, n))
 
 
 def tk_swiglu_per_token_cast_host(x_ptr, M, N, ld_x, group, fmt, mode, layout,
                                   codes_ptr, ld_codes, scales_ptr, ld_scales,
                                   scratch_ptr, scratch_bytes, chunk_rows=0,
-                                  stream0=0, stream1=0) -> None:
+                                  streams=(0,)) -> None:
     """Raw-pointer call of the host-buffer fused SwiGLU cast."""
+    arr, n = _stream_array(streams)
     _check(load().tk_swiglu_per_token_cast_host(
         x_ptr, M, N, ld_x, group, fmt, mode, layout, codes_ptr, ld_codes,
-        scales_ptr, ld_scales, scratch_ptr, scratch_bytes, chunk_rows,
-        stream0, stream1))
+        scales_ptr, ld_scales, scratch_ptr, scratch_bytes, chunk_rows, arr,
+        n))
 
 
 def tk_get_device_fault(clear: bool = False) -> int:
@@ -324,11 +331,17 @@ def _outputs(torch, M, K, group, fmt, scale, layout, device, codes, scales):
 _host_streams = {}
 
 
+HOST_STREAMS = 4    # streams the host-buffer pipeline deals its chunks over
+
+
 def _copy_streams(torch, device):
-    """Two streams per device for the host-buffer pipeline (created once)."""
+    """The host-buffer pipeline's streams for a device (created once), and
+    their handles as a ctypes array."""
     key = torch.device(device).index
     if key not in _host_streams:
-        _host_streams[key] = (torch.cuda.Stream(device), torch.cuda.Stream(device))
+        streams = tuple(torch.cuda.Stream(device) for _ in range(HOST_STREAMS))
+        _host_streams[key] = (streams,
+                              _stream_array([st.cuda_stream for st in streams]))
     return _host_streams[key]
 
 
@@ -367,18 +380,18 @@ def _call_host(entry, torch, x, K, group, fmt, scale, layout, codes, scales):
     device = torch.device("cuda", torch.cuda.current_device())
     need = tk_host_scratch_bytes(M, K, group, FMT[fmt], SCALE[scale],
                                  LAYOUT[layout], int(swiglu))
-    scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
-    s0, s1 = _copy_streams(torch, device)
-    # the scratch comes from the current stream's pool: start after it
-    cur = torch.cuda.current_stream(device)
-    s0.wait_stream(cur)
-    s1.wait_stream(cur)
-    host_entry = (tk_swiglu_per_token_cast_host if swiglu
-                  else tk_per_token_cast_host)
-    host_entry(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt], SCALE[scale],
-               LAYOUT[layout], codes.data_ptr(), codes.stride(0),
-               scales.data_ptr(), scales.stride(0), scratch.data_ptr(), need,
-               0, s0.cuda_stream, s1.cuda_stream)
+    streams, (arr, n) = _copy_streams(torch, device)
+    # The scratch comes from the first pipeline stream's pool: its blocks
+    # were last used by an earlier call, which finished every stream before
+    # returning, so no stream needs to wait for another.
+    with torch.cuda.stream(streams[0]):
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    host_entry = (load().tk_swiglu_per_token_cast_host if swiglu
+                  else load().tk_per_token_cast_host)
+    _check(host_entry(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt],
+                      SCALE[scale], LAYOUT[layout], codes.data_ptr(),
+                      codes.stride(0), scales.data_ptr(), scales.stride(0),
+                      scratch.data_ptr(), need, 0, arr, n))
     return codes, scales
 
 
@@ -391,7 +404,8 @@ def per_token_cast(x, group: int = 128, fmt: str = "e4m3",
     current stream.  CPU input (preferably pinned): the library's host-buffer
     pipeline uploads the rows in chunks to the current CUDA device, casts
     them there and downloads codes and scales into (pinned) host tensors,
-    chunks alternating over two streams; returns once they are on the host.
+    chunks dealt over HOST_STREAMS streams; returns once they are on the
+    host.
     Returns (codes uint8 [M, K or K/2], scales) -- see ``scale_shape``.
     """
     K = x.shape[1]

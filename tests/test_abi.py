@@ -323,11 +323,12 @@ def test_per_channel_workspace_size(lib):
 def call_host(lib, *, x=A, M=4, K=256, ld_x=256, group=128, fmt=0, mode=0,
               layout=0, codes=B, ld_codes=256, scales=C, ld_scales=2,
               scratch=0x40000, scratch_bytes=1 << 20, chunk_rows=0,
-              swiglu=False):
+              n_streams=2, swiglu=False, no_array=False):
     fn = (lib.tk_swiglu_per_token_cast_host if swiglu
           else lib.tk_per_token_cast_host)
+    arr = None if no_array else (ctypes.c_void_p * max(n_streams, 1))()
     return fn(x, M, K, ld_x, group, fmt, mode, layout, codes, ld_codes, scales,
-              ld_scales, scratch, scratch_bytes, chunk_rows, None, None)
+              ld_scales, scratch, scratch_bytes, chunk_rows, arr, n_streams)
 
 
 HOST_CASES = [
@@ -339,6 +340,9 @@ HOST_CASES = [
     ("ld_scales < G", dict(ld_scales=1), INVALID),
     ("transposed ld_scales < M", dict(layout=1, ld_scales=3), INVALID),
     ("negative chunk_rows", dict(chunk_rows=-1), INVALID),
+    ("no streams", dict(n_streams=0), INVALID),
+    ("65 streams", dict(n_streams=65), INVALID),
+    ("null stream array", dict(no_array=True), INVALID),
     ("null x", dict(x=None), INVALID),
     ("null scales", dict(scales=None), INVALID),
     ("null scratch", dict(scratch=None), INVALID),
@@ -358,23 +362,23 @@ def test_host_entry_validation(lib, name, kw, want):
 
 
 def test_host_scratch_size(lib):
-    """Input rows padded to 16 B, code rows to 16 B, row-major scale rows to
-    4 words (transposed: tokens padded to 4), each region rounded up to
+    """Input rows padded to 16 B, code rows to 16 B, row-major scale rows
+    unpadded (transposed: tokens padded to 4), each region rounded up to
     256 B."""
     def r256(v):
         return (v + 255) // 256 * 256
-    # 4096 x 7168 E4M3 g128 UE8M0 row-major: 14 words -> 16
+    # 4096 x 7168 E4M3 g128 UE8M0 row-major: 14 words per row
     assert tk.tk_host_scratch_bytes(4096, 7168, 128, 0, 2, 0, 0) == (
-        4096 * 7168 * 2 + 4096 * 7168 + 4096 * 16 * 4)
+        4096 * 7168 * 2 + 4096 * 7168 + r256(4096 * 14 * 4))
     # SwiGLU 3 x [272 | 272] E2M1 g16 fp32 transposed: 17 scale rows x 4
     assert tk.tk_host_scratch_bytes(3, 272, 16, 1, 0, 1, 1) == (
         r256(3 * 544 * 2) + r256(3 * 144) + r256(17 * 4 * 4))
-    # 5 x 272 E2M1 g16 fp32 row-major: 17 words -> 20
+    # 5 x 272 E2M1 g16 fp32 row-major: 17 words per row
     assert tk.tk_host_scratch_bytes(5, 272, 16, 1, 0, 0, 0) == (
-        r256(5 * 272 * 2) + r256(5 * 144) + r256(5 * 20 * 4))
+        r256(5 * 272 * 2) + r256(5 * 144) + r256(5 * 17 * 4))
     assert tk.tk_host_scratch_bytes(4, 200, 128, 0, 0, 0, 0) == 0   # K % group
     assert tk.tk_host_scratch_bytes(4, 256, 128, 0, 0, 0, 1) == (
-        r256(4 * 512 * 2) + r256(4 * 256) + r256(4 * 4 * 4))
+        r256(4 * 512 * 2) + r256(4 * 256) + r256(4 * 2 * 4))
 
 
 def test_empty_batch_is_a_noop(lib):

@@ -391,7 +391,7 @@ def test_host_entry_chunks_and_strides(layout, chunk_rows, swiglu):
     """The raw host-buffer entry: small and ragged chunks (37 rounds down to
     36), host row strides wider than the rows and not multiples of 16 (the
     input pad poisoned, the output pads filled with a sentinel that must
-    survive), pageable numpy memory, and one stream for both chunk streams.
+    survive), pageable numpy memory, and one stream listed twice.
     Results equal the device-tensor call's bit for bit."""
     import torch
     M, K, group, fmt, mode = 203, 384, 64, "e4m3", "fp32"
@@ -416,7 +416,7 @@ def test_host_entry_chunks_and_strides(layout, chunk_rows, swiglu):
              else tk.tk_per_token_cast_host)
     entry(xh.ctypes.data, M, K, ld_x, group, tk.FMT[fmt], tk.SCALE[mode],
           tk.LAYOUT[layout], codes.ctypes.data, ld_codes, scales.ctypes.data,
-          ld_scales, scratch.data_ptr(), need, chunk_rows, s, s)
+          ld_scales, scratch.data_ptr(), need, chunk_rows, (s, s))
     x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
     fn = tk.swiglu_per_token_cast if swiglu else tk.per_token_cast
     dc, ds = fn(x, group=group, fmt=fmt, scale=mode, layout=layout)
