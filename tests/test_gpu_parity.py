@@ -85,6 +85,34 @@ def test_strides_and_padding(fmt, layout):
         assert_bit_exact(case)
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("mode", ["fp32", "pow2"])
+@pytest.mark.parametrize("group,K", [(16, 256), (16, 512), (32, 512), (32, 1024),
+                                     (16, 2048), (32, 4096)])
+def test_interleaved_rows_transposed(fmt, mode, group, K):
+    """Transposed fp32 / pow2 scales of groups of 16 or 32 with a power of
+    two of whole rows per 16 KiB tile (2 to 32): the kernel interleaves a
+    full tile's rows over lanes.  Batches of full tiles, with a ragged last
+    tile (which takes the plain mapping), and smaller than one tile."""
+    rows = 16384 // (2 * K)
+    for M in (3 * rows + 1, 2 * rows, max(rows - 1, 1)):
+        seed = zlib.crc32(repr((fmt, mode, group, K, M)).encode()) & 0xFFFF
+        bits = random_bf16(seed, M, K, scale=2.0)
+        assert_bit_exact(Case(bits, K, group, fmt, mode, "transposed"))
+
+
+@pytest.mark.parametrize("mode", ["fp32", "pow2"])
+@pytest.mark.parametrize("group,N", [(32, 256), (16, 512), (32, 1024), (32, 2048)])
+def test_interleaved_rows_transposed_swiglu(mode, group, N):
+    """The fused SwiGLU cast on row-interleaved tiles (gate and up halves
+    share a 16 KiB tile: 2 to 16 rows)."""
+    rows = 16384 // (4 * N)
+    for M in (3 * rows + 1, 2 * rows):
+        bits = random_bf16(N + M + group, M, 2 * N, scale=2.0)
+        case = Case(bits, N, group, "e4m3", mode, "transposed", swiglu=True)
+        check_swiglu(case, max_code_frac=2e-3 if M * N < 5000 else 1e-4)
+
+
 def test_empty_batch():
     case = Case(np.zeros((0, 128), np.uint16), 128, 128, "e4m3", "fp32",
                 "row")
