@@ -366,7 +366,8 @@ def _call(entry, x, K, group, fmt, scale, layout, codes, scales, stream):
 
 def _call_host(entry, torch, x, K, group, fmt, scale, layout, codes, scales):
     """CPU tensors: the library's host-buffer pipeline (chunks of rows
-    uploaded, cast and downloaded on two streams) on the current device."""
+    uploaded, cast and downloaded on HOST_STREAMS streams) on the current
+    device."""
     M = x.shape[0]
     swiglu = entry is tk_swiglu_per_token_cast
     if codes is None:
