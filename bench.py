@@ -500,9 +500,10 @@ def run_gpu(args):
 
 
 def run_e2e(torch, tk, w, steps, device, world):
-    """Same metric through the public API with host buffers: each step copies
-    the pinned host input to the device, casts, and copies codes and scales
-    back to pinned host memory (all inside the timed interval)."""
+    """Same metric through the public API with host buffers: each step the
+    library's host-buffer entry uploads the pinned host input to the device
+    in chunks, casts them, and downloads codes and scales to pinned host
+    memory (all inside the timed interval)."""
     bits = make_input(w)
     xh = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
     xh = xh.pin_memory()
@@ -528,7 +529,9 @@ def run_e2e(torch, tk, w, steps, device, world):
             "d2h_bytes_per_step": int(codes.numel() + scales.numel() * 4),
             "api": ("precision_quantization_token_gb300."
                     + ("swiglu_per_token_cast" if w.swiglu
-                       else "per_token_cast") + " on pinned host tensors")}
+                       else "per_token_cast") + " on pinned host tensors "
+                    "(C entry tk_" + ("swiglu_" if w.swiglu else "")
+                    + "per_token_cast_host)")}
 
 
 # ------------------------------------------------------------- CPU arm
