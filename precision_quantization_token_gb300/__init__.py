@@ -329,6 +329,8 @@ def _outputs(torch, M, K, group, fmt, scale, layout, device, codes, scales):
 
 
 _host_streams = {}
+_host_scratch = {}
+_host_lock = threading.Lock()
 
 
 HOST_STREAMS = 4    # streams the host-buffer pipeline deals its chunks over
@@ -382,17 +384,25 @@ def _call_host(entry, torch, x, K, group, fmt, scale, layout, codes, scales):
     need = tk_host_scratch_bytes(M, K, group, FMT[fmt], SCALE[scale],
                                  LAYOUT[layout], int(swiglu))
     streams, (arr, n) = _copy_streams(torch, device)
-    # The scratch comes from the first pipeline stream's pool: its blocks
-    # were last used by an earlier call, which finished every stream before
-    # returning, so no stream needs to wait for another.
-    with torch.cuda.stream(streams[0]):
-        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
     host_entry = (load().tk_swiglu_per_token_cast_host if swiglu
                   else load().tk_per_token_cast_host)
-    _check(host_entry(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt],
-                      SCALE[scale], LAYOUT[layout], codes.data_ptr(),
-                      codes.stride(0), scales.data_ptr(), scales.stride(0),
-                      scratch.data_ptr(), need, 0, arr, n))
+    # One scratch per device, grown on demand and reused: the call returns
+    # only after every stream it used is idle, and the lock keeps two host
+    # threads from sharing it at once.
+    with _host_lock:
+        scratch = _host_scratch.get(device.index)
+        if scratch is None or scratch.numel() < need:
+            torch.cuda.synchronize(device)
+            _host_scratch.pop(device.index, None)
+            with torch.cuda.stream(streams[0]):
+                scratch = torch.empty(max(need, 16), dtype=torch.uint8,
+                                      device=device)
+            _host_scratch[device.index] = scratch
+        _check(host_entry(x.data_ptr(), M, K, x.stride(0), group, FMT[fmt],
+                          SCALE[scale], LAYOUT[layout], codes.data_ptr(),
+                          codes.stride(0), scales.data_ptr(),
+                          scales.stride(0), scratch.data_ptr(), need, 0, arr,
+                          n))
     return codes, scales
 
 
@@ -406,7 +416,8 @@ def per_token_cast(x, group: int = 128, fmt: str = "e4m3",
     pipeline uploads the rows in chunks to the current CUDA device, casts
     them there and downloads codes and scales into (pinned) host tensors,
     chunks dealt over HOST_STREAMS streams; returns once they are on the
-    host.
+    host.  The device scratch it stages through (the largest needed so
+    far) is kept per device for later calls.
     Returns (codes uint8 [M, K or K/2], scales) -- see ``scale_shape``.
     """
     K = x.shape[1]
