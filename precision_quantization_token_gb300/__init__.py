@@ -383,13 +383,13 @@ def _call_host(entry, torch, x, K, group, fmt, scale, layout, codes, scales):
     device = torch.device("cuda", torch.cuda.current_device())
     need = tk_host_scratch_bytes(M, K, group, FMT[fmt], SCALE[scale],
                                  LAYOUT[layout], int(swiglu))
-    streams, (arr, n) = _copy_streams(torch, device)
     host_entry = (load().tk_swiglu_per_token_cast_host if swiglu
                   else load().tk_per_token_cast_host)
     # One scratch per device, grown on demand and reused: the call returns
     # only after every stream it used is idle, and the lock keeps two host
-    # threads from sharing it at once.
+    # threads from sharing it (or the streams) at once.
     with _host_lock:
+        streams, (arr, n) = _copy_streams(torch, device)
         scratch = _host_scratch.get(device.index)
         if scratch is None or scratch.numel() < need:
             torch.cuda.synchronize(device)
