@@ -39,6 +39,26 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(raw, n), n
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/*.h is a C ABI: a C99 translation unit (all warnings as
+    errors) includes it and takes the address of every declared function."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "abi_check.c"
+    src.write_text('#include "tk_cast.h"\n'
+                   "void *table[] = {\n" +
+                   "".join(f"    (void *)&{n},\n" for n in names) +
+                   "};\n")
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror",
+                        "-Wno-pedantic", "-fsyntax-only",
+                        f"-I{os.path.join(ROOT, 'include')}", str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_status_strings(lib):
     assert tk.tk_status_string(0) == "TK_OK"
     assert tk.tk_status_string(3) == "TK_ERR_MISALIGNED"
